@@ -1,0 +1,137 @@
+/* msa.h -- C ABI of libmsa: the MiniMax Sparse Attention (MSA) forward pass on
+ * one GB300 (sm_103a).
+ *
+ * What is computed ("MiniMax 模型迭代与竞品分析：从 Text-01、M1、M2 到 M3",
+ * section 2 "从 Lightning Attention 到 MSA", inference steps 1-4):
+ *   1. per GQA group g, a light index query Q_idx[t,g] is scored against the
+ *      index key K_idx[i] that all groups share, for every causal token i;
+ *   2. token scores are max-pooled into 128-token KV blocks;
+ *   3. 16 blocks are selected per (query, group), the query's own (local)
+ *      block lb = t/128 forced in as one of the 16;
+ *   4. every query head of the group runs exact softmax attention
+ *      (s = q.k * scale, softmax over the attended tokens, o = sum p v; the
+ *      full-attention equation of the same section) over the tokens <= t of
+ *      the selected blocks only, at most 16*128 = 2048 tokens.
+ * The KV cache is block-major, block -> token -> head -> dim
+ * ("前沿架构解码手记（三）：MiniMax M2.7 → M3", section 2.1 "KV-Block-Major").
+ *
+ * Readings fixed by this library where the pages are silent: the index score
+ * is the raw dot product (no scale, no activation), ranked without exp; ties
+ * between equal pooled scores go to the lower block id; with fewer than 16
+ * causal blocks all lb+1 are selected; selected ids are written ascending
+ * and padded with -1; one softmax spans all selected tokens of a head.
+ *
+ * Conventions for every entry point:
+ *   - bf16 tensors are passed as uint16_t bit patterns in DEVICE memory that
+ *     the caller owns; layouts are row-major, innermost index last:
+ *       q_idx   [B][T][G][Di]           k_idx   [B][max_blocks*128][Di]
+ *       q, out  [B][T][H][D]            k_cache, v_cache [B][max_blocks][128][G][D]
+ *       sel     [B][T][G][16] int32     (device)
+ *     Query head h belongs to group g = h / (H/G) and reads KV head g.
+ *   - q_start and kv_len are HOST arrays of B int32: query i of sequence b
+ *     sits at absolute position q_start[b] + i, and the causal context of
+ *     sequence b is its first kv_len[b] tokens.  Required:
+ *     0 <= q_start[b], q_start[b] + T <= kv_len[b] <= max_blocks*128.
+ *     Prefill: q_start = 0, kv_len = T.  Chunked prefill: q_start = chunk
+ *     start.  Decode: T = 1, q_start = kv_len - 1 (the new token's K, V and
+ *     K_idx are already in the caches).
+ *   - ws is caller-owned device scratch of at least msa_workspace_bytes(p)
+ *     bytes, 256-byte aligned.  The library never allocates memory and keeps
+ *     no state between calls except a status word inside ws.
+ *   - Work is enqueued asynchronously on `stream`; nothing synchronises.
+ *     Inputs must stay valid until the stream reaches the call's end.
+ *   - Every entry point returns MSA_OK or a negative msa_status.  Argument
+ *     errors are found on the host before anything is enqueued.  A kernel
+ *     whose bounded wait runs out records MSA_ERR_TIMEOUT in ws; read it with
+ *     msa_workspace_status().
+ *   - Supported shapes: block == 128, topk == 16, H % G == 0, D in {64, 128},
+ *     Di in {32, 64}, 1 <= B <= MSA_MAX_BATCH, T >= 0 (T == 0 is a no-op).
+ *     Others return MSA_ERR_UNSUPPORTED.
+ *   - Pointers must be 16-byte aligned (MSA_ERR_INVALID_ARG otherwise).
+ */
+#ifndef MSA_H
+#define MSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MSA_BLOCK 128
+#define MSA_TOPK 16
+#define MSA_MAX_BATCH 256
+
+typedef enum {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = -1, /* null/misaligned pointer, inconsistent sizes    */
+  MSA_ERR_UNSUPPORTED = -2, /* a shape outside the supported set              */
+  MSA_ERR_WORKSPACE = -3,   /* ws too small                                   */
+  MSA_ERR_CUDA = -4,        /* a CUDA launch or driver call failed            */
+  MSA_ERR_TIMEOUT = -5      /* a kernel's bounded wait ran out (read from ws) */
+} msa_status;
+
+/* Which kernels run the prefill steps.  MSA_KERNELS_AUTO picks by shape: the
+ * tensor-core (tcgen05) index scan and KV-outer attention for prefill-sized
+ * T, the per-query streaming kernels for decode-sized T.  The two forced
+ * values exist so that tests can exercise both families on any shape. */
+typedef enum {
+  MSA_KERNELS_AUTO = 0,
+  MSA_KERNELS_STREAMING = 1,
+  MSA_KERNELS_TENSORCORE = 2
+} msa_kernels;
+
+typedef struct {
+  int B;          /* sequences in the call                                  */
+  int T;          /* query tokens per sequence in the call                  */
+  int H;          /* query heads                                            */
+  int G;          /* GQA groups = KV heads                                  */
+  int D;          /* head dim of q, k, v                                    */
+  int Di;         /* index dim of q_idx, k_idx                              */
+  int block;      /* tokens per KV block, must be MSA_BLOCK                 */
+  int topk;       /* blocks per (query, group), must be MSA_TOPK            */
+  int max_blocks; /* block capacity of each sequence's caches               */
+  float scale;    /* main-branch softmax scale, normally 1/sqrt(D)          */
+  int kernels;    /* an msa_kernels value                                   */
+} msa_params;
+
+/* Bytes of device scratch the entry points need for these params (the
+ * maximum over msa_index_topk, msa_sparse_attn and msa_forward). */
+size_t msa_workspace_bytes(const msa_params *p);
+
+/* Steps 1-3.  Writes sel[B][T][G][16]: the selected block ids of each
+ * (query, group), ascending, -1 padded; always min(16, lb+1) ids including
+ * lb.  Index scores accumulate in fp32; they are exact when Q_idx and K_idx
+ * products and sums fit fp32 exactly (e.g. values on a 2^-3 grid). */
+int msa_index_topk(const msa_params *p, const uint16_t *q_idx, const uint16_t *k_idx,
+                   const int32_t *q_start, const int32_t *kv_len, int32_t *sel,
+                   void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Step 4 for a caller-given selection sel[B][T][G][16] (ids ascending or
+ * not, -1 entries ignored, every id in [0, lb]).  Writes out[B][T][H][D]
+ * bf16 (round to nearest even) from fp32 accumulation. */
+int msa_sparse_attn(const msa_params *p, const uint16_t *q, const uint16_t *k_cache,
+                    const uint16_t *v_cache, const int32_t *sel, const int32_t *q_start,
+                    const int32_t *kv_len, uint16_t *out, void *ws, size_t ws_bytes,
+                    cudaStream_t stream);
+
+/* Steps 1-4.  sel_out may be NULL (the selection then lives in ws). */
+int msa_forward(const msa_params *p, const uint16_t *q_idx, const uint16_t *k_idx,
+                const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                const int32_t *q_start, const int32_t *kv_len, int32_t *sel_out,
+                uint16_t *out, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Waits for `stream`, then returns the status the last call on ws left in
+ * it: MSA_OK, or MSA_ERR_TIMEOUT if a kernel's bounded wait ran out (its
+ * outputs are then incomplete).  MSA_ERR_CUDA if the read itself fails. */
+int msa_workspace_status(const void *ws, cudaStream_t stream);
+
+/* A static, human-readable name of a status code. */
+const char *msa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MSA_H */

@@ -1,0 +1,81 @@
+/* MSA CPU oracle -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, double-precision restatement of what the MiniMax Sparse
+ * Attention (MSA) forward pass computes, written from the description in
+ * "MiniMax 模型迭代与竞品分析：从 Text-01、M1、M2 到 M3", section 2
+ * ("从 Lightning Attention 到 MSA"): the full-attention equation and the four
+ * inference steps (global index scoring, 128-token max pooling, top-16 with
+ * the local block forced in, exact softmax over the selected blocks).
+ *
+ * Only tests, the smoke check and the benchmark's CPU-baseline leg may load
+ * this library.  It shares no code with the CUDA path.
+ *
+ * Tensors are bf16 bit patterns (uint16_t) in the library's layouts:
+ *   q_idx [B][T][G][Di]     k_idx [B][cap][Di]      (cap = max_blocks*block)
+ *   q     [B][T][H][D]      k, v  [B][max_blocks][block][G][D]
+ *   sel   [B][T][G][topk]   ascending block ids, -1 padded
+ *   out   [B][T][H][D]      double
+ * Query i of sequence b sits at absolute position t = q_start[b] + i.
+ */
+#ifndef MSA_REF_H
+#define MSA_REF_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+  int H;         /* query heads                                  */
+  int G;         /* GQA groups = KV heads; heads of group g are  */
+                 /* [g*H/G, (g+1)*H/G)                           */
+  int D;         /* head dim of q, k, v                          */
+  int Di;        /* index dim of q_idx, k_idx                    */
+  int block;     /* tokens per KV block (128)                    */
+  int topk;      /* blocks selected per (query, group) (16)      */
+  double scale;  /* main-branch softmax scale (1/sqrt(D))        */
+} msa_ref_dims;
+
+/* Status: 0 ok, -1 bad argument. */
+
+/* Index branch for one query at absolute position t of one sequence.
+ * q_idx_t [G][Di]; k_idx [>= t+1][Di]; sel_t [G][topk] (output).
+ * pooled (optional, may be NULL): [G][t/block] pooled scores of the
+ * candidate blocks. */
+int msa_ref_select(const msa_ref_dims *p, int64_t t, const uint16_t *q_idx_t,
+                   const uint16_t *k_idx, int32_t *sel_t, double *pooled);
+
+/* Main branch for one query: exact softmax attention of every head over the
+ * tokens of its group's selected blocks that are <= t.
+ * q_t [H][D]; k, v [nblocks][block][G][D]; sel_t [G][topk]; out_t [H][D]. */
+int msa_ref_attend(const msa_ref_dims *p, int64_t t, const uint16_t *q_t,
+                   const uint16_t *k, const uint16_t *v, const int32_t *sel_t,
+                   double *out_t);
+
+/* Dense causal GQA attention for one query over all tokens <= t (no
+ * selection); the special case MSA must reduce to when t < topk*block. */
+int msa_ref_dense(const msa_ref_dims *p, int64_t t, const uint16_t *q_t,
+                  const uint16_t *k, const uint16_t *v, double *out_t);
+
+/* Batched forms over the library layouts, OpenMP over queries when
+ * nthreads > 1.  kv_len[b] bounds the causal context: q_start[b] + T <=
+ * kv_len[b] <= max_blocks*block. */
+int msa_ref_index_topk(const msa_ref_dims *p, int B, int T, int max_blocks,
+                       const uint16_t *q_idx, const uint16_t *k_idx,
+                       const int32_t *q_start, const int32_t *kv_len,
+                       int32_t *sel, int nthreads);
+
+int msa_ref_sparse_attn(const msa_ref_dims *p, int B, int T, int max_blocks,
+                        const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        const int32_t *sel, const int32_t *q_start,
+                        const int32_t *kv_len, double *out, int nthreads);
+
+int msa_ref_dense_attn(const msa_ref_dims *p, int B, int T, int max_blocks,
+                       const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const int32_t *q_start, const int32_t *kv_len,
+                       double *out, int nthreads);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

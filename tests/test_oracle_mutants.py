@@ -1,0 +1,78 @@
+"""Plant plausible mistakes in copies of the CPU oracle and require the pins to
+catch each one.  Mutants are compiled from text-edited copies of
+oracle/msa_ref.c into a temporary directory; the committed oracle is untouched.
+"""
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import test_oracle as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "msa_ref.c")
+
+MUTANTS = {
+    # tie rule reversed: equal pooled scores rank the higher block id first
+    "tie_reversed": ("return (x->blk > y->blk) - (x->blk < y->blk);",
+                     "return (x->blk < y->blk) - (x->blk > y->blk);"),
+    # min pooling instead of max pooling
+    "min_pool": ("if (s > best) best = s;", "if (best == -INFINITY || s < best) best = s;"),
+    # sum pooling instead of max pooling
+    "sum_pool": ("if (s > best) best = s;", "best = (best == -INFINITY ? 0.0 : best) + s;"),
+    # local block counted on top of the topk (17 instead of 16)
+    "local_extra": ("int64_t nsel = lb + 1 < p->topk ? lb + 1 : p->topk;",
+                    "int64_t nsel = lb + 1 < p->topk + 1 ? lb + 1 : p->topk + 1;"),
+    # causal clip of the local block dropped
+    "no_causal_clip": ("if (tok > t) continue;", "(void)0;"),
+    # softmax scale dropped
+    "no_scale": ("z[i] = s * p->scale;", "z[i] = s;"),
+    # wrong KV head for a query head (reversed group order)
+    "wrong_kv_head": ("krow[n] = k + (size_t)tok * row + (size_t)g * p->D;\n          vrow",
+                      "krow[n] = k + (size_t)tok * row + (size_t)(p->G - 1 - g) * p->D;\n          vrow"),
+    # index dot product over one dimension too few
+    "dropped_index_term": ("for (int d = 0; d < p->Di; ++d) s +=",
+                           "for (int d = 1; d < p->Di; ++d) s +="),
+    # softmax normaliser off by one
+    "bad_normaliser": ("for (int d = 0; d < D; ++d) out[d] /= l;",
+                       "for (int d = 0; d < D; ++d) out[d] /= (l + 1.0);"),
+}
+
+PINS = [
+    lambda r: pins.test_selection_equals_bruteforce_small_blocks(r, 4, 5, 3, 2),
+    lambda r: pins.test_selection_equals_bruteforce_small_blocks(r, 8, 6, 4, 8),
+    pins.test_selection_equals_bruteforce_block128,
+    pins.test_needle_block_is_selected,
+    pins.test_short_context_equals_full_causal_attention,
+    pins.test_sparse_equals_masked_sdpa,
+    pins.test_closed_forms,
+]
+
+
+@pytest.fixture(scope="module")
+def mutant_dir(tmp_path_factory):
+    return tmp_path_factory.mktemp("mutants")
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, mutant_dir):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, "mutation site must exist exactly once"
+    d = mutant_dir / name
+    d.mkdir()
+    shutil.copy(os.path.join(os.path.dirname(SRC), "msa_ref.h"), d / "msa_ref.h")
+    (d / "msa_ref.c").write_text(text.replace(old, new))
+    so = str(d / "libmut.so")
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared",
+                           str(d / "msa_ref.c"), "-o", so, "-lm"])
+    caught = []
+    with oracle.use_library(so):
+        for pin in PINS:
+            try:
+                pin(oracle)
+            except (AssertionError, ValueError):
+                caught.append(pin)
+    assert caught, "mutant %s passed every pin" % name
