@@ -1,0 +1,469 @@
+#!/usr/bin/env python
+"""Benchmark of the MSA forward pass (libmsa) on GB300.
+
+One step = the whole hot path (index scoring, block max-pooling, top-16 with
+the local block forced, sparse softmax attention) over one batch of seeded
+synthetic inputs already resident in HBM:
+
+  decode_256k   64 sequences x 262144-token block-major caches, 1 new query
+                each (48 query / 8 KV heads, D 128, Di 64)
+  prefill_128k  one 131072-token sequence, one call
+  prefill_1m    one 1,048,576-token sequence, 128 chunked calls of 8192 queries
+  prefill_32k   one 32768-token sequence
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle (the
+reference arm) on a bounded sample of the same workload instead.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MSA prefill & decode tokens/s at 128K–1M ctx; % of TC/HBM roofline"
+H, G, D, DI, BLK = 48, 8, 128, 64, 128
+WORKLOADS = {
+    "prefill_32k": dict(cfg=1, kind="prefill", B=1, L=32768, chunk=32768),
+    "prefill_128k": dict(cfg=2, kind="prefill", B=1, L=131072, chunk=131072),
+    "decode_256k": dict(cfg=3, kind="decode", B=64, L=262144),
+    "prefill_1m": dict(cfg=4, kind="prefill", B=1, L=1048576, chunk=8192),
+}
+DEFAULT_WORKLOAD = "decode_256k"
+
+
+# ------------------------------------------------------------ algorithmic work --
+def lb_of(t):
+    return t // BLK
+
+
+def attended_tokens(t):
+    """Tokens the main branch attends for query position(s) t."""
+    t = np.asarray(t, np.int64)
+    return np.where(t < 16 * BLK, t + 1, 15 * BLK + t % BLK + 1)
+
+
+def index_flops(t):
+    """2*Di*G per scored (query, group, key); keys = the lb*128 candidate tokens."""
+    t = np.asarray(t, np.int64)
+    return float(np.sum(2.0 * DI * G * BLK * (t // BLK)))
+
+
+def attn_flops(t):
+    return float(np.sum(4.0 * D * H * attended_tokens(t)))
+
+
+def decode_bytes(B, L):
+    t = L - 1
+    kidx = B * lb_of(t) * BLK * DI * 2                     # candidate blocks' K_idx
+    kv = B * G * int(attended_tokens(t)) * D * 2 * 2       # gathered K and V
+    small = B * (H * D * 2 * 2 + G * DI * 2 + G * 16 * 4)  # q, out, q_idx, sel
+    return kidx, kv + small
+
+
+# --------------------------------------------------------------------- clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu):
+        self.rows, self.proc = [], None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if not self.rows:
+            return None
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in self.rows for k in range(4)
+                          if r[5 + k].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+# ------------------------------------------------------------- distributed --
+def dist_setup(gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ GPU arm --
+class Job:
+    """Device inputs and the sequence of C-ABI calls that make one step."""
+
+    def __init__(self, name, rank):
+        import torch
+        import block_sparse_attention_04_gb300 as msa
+        import msa_synth.device as sd
+        self.msa = msa
+        self.name, self.w = name, WORKLOADS[name]
+        w = self.w
+        self.B, self.L = w["B"], w["L"]
+        self.nb = self.L // BLK
+        self.seed = 20261202 + w["cfg"]
+        b0 = rank * self.B
+        if w["kind"] == "decode":
+            self.calls = [dict(T=1, q_start=[self.L - 1] * self.B, kv_len=[self.L] * self.B,
+                               qoff=0)]
+            qrows = (self.L - 1, self.L)
+        else:
+            c = w["chunk"]
+            self.calls = [dict(T=c, q_start=[s], kv_len=[s + c], qoff=s)
+                          for s in range(0, self.L, c)]
+            qrows = (0, self.L)
+        self.dev = sd.make_inputs(self.B, H, G, D, DI, self.nb, self.L, self.seed, q_rows=qrows,
+                                  b0=b0)
+        T = self.calls[0]["T"]
+        self.params = msa.params(self.B, T, H, G, D, DI, self.nb)
+        self.ws = msa.workspace(self.params)
+        self.sel = torch.empty((self.B, qrows[1] - qrows[0], G, 16), dtype=torch.int32,
+                               device="cuda")
+        self.out = torch.empty((self.B, qrows[1] - qrows[0], H, D), dtype=torch.int16,
+                               device="cuda")
+        torch.cuda.synchronize()
+
+    def views(self, c, dev=None, sel=None, out=None):
+        dev = dev or self.dev
+        sel = self.sel if sel is None else sel
+        out = self.out if out is None else out
+        a, T = c["qoff"], c["T"]
+        return (dev["q_idx"][:, a:a + T], dev["k_idx"], dev["q"][:, a:a + T], dev["k"], dev["v"],
+                sel[:, a:a + T], out[:, a:a + T])
+
+    def step(self, ev=None):
+        """Enqueue one step; ev: list to which (start, mid, end) events are appended."""
+        import torch
+        msa = self.msa
+        for c in self.calls:
+            q_idx, k_idx, q, k, v, sel, out = self.views(c)
+            if ev is not None:
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                e[0].record()
+            msa.msa_index_topk(self.params, q_idx, k_idx, c["q_start"], c["kv_len"], sel, self.ws)
+            if ev is not None:
+                e[1].record()
+            msa.msa_sparse_attn(self.params, q, k, v, sel, c["q_start"], c["kv_len"], out,
+                                self.ws)
+            if ev is not None:
+                e[2].record()
+                ev.append(e)
+
+    def tokens(self):
+        return self.B * (1 if self.w["kind"] == "decode" else self.L)
+
+    def positions(self):
+        if self.w["kind"] == "decode":
+            return np.full(self.B, self.L - 1, np.int64)
+        return np.arange(self.L, dtype=np.int64)
+
+
+def time_job(job, steps, warmup, world):
+    import torch
+    for _ in range(warmup):
+        job.step()
+    job.msa.msa_workspace_status(job.ws)
+    torch.cuda.synchronize()
+    n0 = job.msa.msa_kernel_launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    time.sleep(0.3)
+    ev = []
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        job.step(ev)
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ck = clocks.stop()
+    launches = job.msa.msa_kernel_launch_count() - n0
+    job.msa.msa_workspace_status(job.ws)
+    total_ms = t0.elapsed_time(t1)
+    idx_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    att_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    return max_over_ranks(total_ms, world), idx_ms, att_ms, launches, ck
+
+
+def time_e2e(job, steps, world):
+    """Same step through the C ABI with host buffers: pinned H2D of the step's
+    inputs and D2H of its outputs inside the timed region."""
+    import torch
+    if job.w["kind"] == "decode":
+        names = ["q_idx", "q"]      # the caches stay resident between decode steps
+    else:
+        names = ["q_idx", "k_idx", "q", "k", "v"]
+    host = {n: torch.empty(job.dev[n].shape, dtype=torch.int16, pin_memory=True) for n in names}
+    for n in names:
+        host[n].copy_(job.dev[n])
+    sel_h = torch.empty(job.sel.shape, dtype=torch.int32, pin_memory=True)
+    out_h = torch.empty(job.out.shape, dtype=torch.int16, pin_memory=True)
+    h2d = sum(host[n].numel() * 2 for n in names)
+    d2h = sel_h.numel() * 4 + out_h.numel() * 2
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        for n in names:
+            job.dev[n].copy_(host[n], non_blocking=True)
+        job.step()
+        sel_h.copy_(job.sel, non_blocking=True)
+        out_h.copy_(job.out, non_blocking=True)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1), world) / steps
+    return ms, h2d, d2h
+
+
+# ---------------------------------------------------------------- CPU arm --
+class OracleSample:
+    """The CPU oracle on a bounded, seeded sample of workload `name`.
+
+    Inputs are generated once (outside the timed region); run() times the
+    oracle's selection and attention for the sampled query rows."""
+
+    def __init__(self, name, rows=None, nthreads=None):
+        import msa_synth as syn
+        import oracle
+        self.syn, self.oracle = syn, oracle
+        w = WORKLOADS[name]
+        self.seed = 20261202 + w["cfg"]
+        self.nthreads = nthreads or (os.cpu_count() or 1)
+        self.d = oracle.dims(H, G, D, DI)
+        self.nb = w["L"] // BLK
+        rng = np.random.default_rng(self.seed)
+        if w["kind"] == "decode":
+            nseq = rows or 16
+            t = w["L"] - 1
+            self.rows = [(b, t) for b in range(nseq)]
+            self.desc = ("%d of the 64 decode sequences (query at position %d), all groups "
+                         "and heads" % (nseq, t))
+        else:
+            nrows = rows or 24
+            ts = np.sort(rng.choice(w["L"], size=nrows, replace=False))
+            self.rows = [(0, int(t)) for t in ts]
+            self.desc = ("%d query positions drawn uniformly from the %d of the sequence, all "
+                         "groups and heads" % (nrows, w["L"]))
+        L = w["L"]
+        self.kidx = {b: syn.kidx_seq(self.seed, b, L, DI) for b in sorted({b for b, _ in self.rows})}
+        self.qidx = {r: syn.qidx_rows(self.seed, r[0], r[1], r[1] + 1, G, DI)[0] for r in self.rows}
+        self.q = {r: syn.q_rows(self.seed, r[0], r[1], r[1] + 1, H, D)[0] for r in self.rows}
+        self.kv = {}
+
+    def _kv(self, row, sel):
+        if row not in self.kv:
+            syn = self.syn
+            blocks = sorted({int(x) for x in sel.reshape(-1) if x >= 0})
+            kc = np.zeros((self.nb, BLK, G, D), np.uint16)
+            vc = np.zeros((self.nb, BLK, G, D), np.uint16)
+            kc[blocks] = syn.kv_blocks(self.seed, syn.TID_K, row[0], blocks, G, D)
+            vc[blocks] = syn.kv_blocks(self.seed, syn.TID_V, row[0], blocks, G, D)
+            self.kv[row] = (kc, vc)
+        return self.kv[row]
+
+    def run(self):
+        """Returns (tokens_per_s, timed seconds)."""
+        from concurrent.futures import ThreadPoolExecutor
+        o, d = self.oracle, self.d
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(self.nthreads) as ex:
+            sels = list(ex.map(lambda r: o.select(d, r[1], self.qidx[r], self.kidx[r[0]]),
+                               self.rows))
+        secs = time.perf_counter() - t0
+        kvs = [self._kv(r, s) for r, s in zip(self.rows, sels)]   # not timed
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(self.nthreads) as ex:
+            list(ex.map(lambda a: o.attend(d, a[0][1], self.q[a[0]], a[1][0], a[1][1], a[2]),
+                        zip(self.rows, kvs, sels)))
+        secs += time.perf_counter() - t0
+        return len(self.rows) / secs, secs
+
+
+def reference_arm(args, world, rank):
+    if rank != 0:
+        return
+    name = args.workload
+    w = WORKLOADS[name]
+    smp = OracleSample(name, rows=args.ref_rows)
+    for _ in range(args.warmup):
+        smp.run()
+    vals, secs = [], 0.0
+    for _ in range(args.steps):
+        v, s = smp.run()
+        vals.append(v)
+        secs += s
+    value = len(smp.rows) * args.steps / secs
+    threads, desc = smp.nthreads, smp.desc
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * secs / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "batch": w["B"], "ctx": w["L"], "heads": H,
+                   "kv_heads": G, "head_dim": D, "index_dim": DI},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def gpu_arm(args, world, rank):
+    import torch
+    import block_sparse_attention_04_gb300 as msa
+    msa.load()
+    peaks, peak_kind = measured_peaks()
+    job = Job(args.workload, rank)
+    total_ms, idx_ms, att_ms, launches, clocks = time_job(job, args.steps, args.warmup, world)
+    ms = total_ms / args.steps
+    tokens = job.tokens() * world
+    value = tokens / (ms / 1000.0)
+    w = job.w
+    pos = job.positions()
+    if w["kind"] == "decode":
+        kidx_b, rest_b = decode_bytes(job.B, job.L)
+        roof = {"bound": "hbm", "kernel": "index scan (msa_index_topk: index_stream + topk_merge)",
+                "achieved": kidx_b / (idx_ms / 1000.0) / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "traffic": None, "peak_kind": peak_kind}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        whole = {"bytes_per_step": kidx_b + rest_b,
+                 "achieved_gbs": (kidx_b + rest_b) / (ms / 1000.0) / 1e9}
+        whole["frac_of_hbm"] = whole["achieved_gbs"] / peaks["hbm_gbs"]
+    else:
+        fi = index_flops(pos) * job.B
+        fa = attn_flops(pos) * job.B
+        peak_tf = peaks["bf16_tflops_sustained"] if ms > 1000 else peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "kernel": "index scan (msa_index_topk)",
+                "achieved": fi / (idx_ms / 1000.0) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
+                "traffic": None, "peak_kind": peak_kind}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        whole = {"flops_per_step": fi + fa, "index_flops": fi, "attn_flops": fa,
+                 "achieved_tflops": (fi + fa) / (ms / 1000.0) / 1e12,
+                 "attn_achieved_tflops": fa / (att_ms / 1000.0) / 1e12}
+        whole["frac_of_bf16_peak"] = whole["achieved_tflops"] / peak_tf
+    e2e_ms, h2d, d2h = time_e2e(job, max(1, min(args.steps, 3)), world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        smp = OracleSample(args.workload)
+        v, secs = smp.run()
+        cpu = {"value": v, "unit": "tokens/s", "cores": smp.nthreads, "kind": "oracle",
+               "sample": smp.desc, "seconds": secs}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded msa_synth generator: Irwin-Hall normals, 2^-3 index grid "
+                "with needles)",
+        "config": {"workload": args.workload, "batch": job.B, "ctx": job.L,
+                   "calls_per_step": len(job.calls), "queries_per_call": job.calls[0]["T"],
+                   "heads": H, "kv_heads": G, "head_dim": D, "index_dim": DI, "block": BLK,
+                   "topk": 16, "l2": "inputs larger than L2 (no flush)"},
+        "roofline": roof, "step": whole,
+        "kernels_ms": {"index_topk": idx_ms, "sparse_attn": att_ms},
+        "e2e": {"value": tokens / (e2e_ms / 1000.0), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--ref-rows", type=int, default=None,
+                    help="rows of the bounded oracle sample per reference step")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        import oracle
+        oracle.build()
+        reference_arm(args, world, rank)
+        return
+    from block_sparse_attention_04_gb300 import _build
+    import msa_synth.device as sd
+    _build.build()
+    sd.build()
+    world, rank, _ = dist_setup(args.gpus)
+    gpu_arm(args, world, rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

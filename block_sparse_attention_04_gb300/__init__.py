@@ -1,0 +1,149 @@
+"""MiniMax Sparse Attention (MSA) forward on GB300: Python binding of libmsa.
+
+Argument marshalling only.  Every step of the path runs in the CUDA kernels
+of libmsa.so (include/msa.h); there is no fallback.  If the library is not
+built, loading raises.  Tensors are torch CUDA tensors with 2-byte elements
+(bf16, int16 or uint16 holding bf16 bit patterns) in the layouts msa.h
+states; q_start and kv_len are host sequences of B ints.
+"""
+import ctypes
+import math
+import os
+
+from . import _build
+
+__all__ = ["MsaParams", "MsaError", "params", "load", "msa_workspace_bytes", "msa_index_topk",
+           "msa_sparse_attn", "msa_forward", "msa_workspace_status", "msa_status_string",
+           "msa_kernel_launch_count",
+           "workspace", "BLOCK", "TOPK"]
+
+BLOCK = 128
+TOPK = 16
+KERNELS = {"auto": 0, "streaming": 1, "tensorcore": 2}
+EXPORTS = ("msa_workspace_bytes", "msa_index_topk", "msa_sparse_attn", "msa_forward",
+           "msa_workspace_status", "msa_status_string", "msa_kernel_launch_count")
+
+
+class MsaError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s failed: %s (%d)" % (what, msa_status_string(status), status))
+
+
+class MsaParams(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
+                ("G", ctypes.c_int), ("D", ctypes.c_int), ("Di", ctypes.c_int),
+                ("block", ctypes.c_int), ("topk", ctypes.c_int), ("max_blocks", ctypes.c_int),
+                ("scale", ctypes.c_float), ("kernels", ctypes.c_int)]
+
+
+def params(B, T, H, G, D, Di, max_blocks, scale=None, kernels="auto"):
+    return MsaParams(B, T, H, G, D, Di, BLOCK, TOPK, max_blocks,
+                     1.0 / math.sqrt(D) if scale is None else scale,
+                     KERNELS[kernels] if isinstance(kernels, str) else int(kernels))
+
+
+_lib = None
+
+
+def load(path=None):
+    """Load libmsa.so (built in-tree by _build.build()); raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or _build.LIBMSA
+    if not os.path.exists(path):
+        raise RuntimeError("libmsa.so is not built (%s); run __graft_entry__.build()" % path)
+    L = ctypes.CDLL(path)
+    P, ci, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    PP = ctypes.POINTER(MsaParams)
+    L.msa_workspace_bytes.argtypes = [PP]
+    L.msa_workspace_bytes.restype = sz
+    L.msa_index_topk.argtypes = [PP, P, P, P, P, P, P, sz, P]
+    L.msa_sparse_attn.argtypes = [PP, P, P, P, P, P, P, P, P, sz, P]
+    L.msa_forward.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, sz, P]
+    L.msa_workspace_status.argtypes = [P, P]
+    L.msa_kernel_launch_count.argtypes = []
+    L.msa_kernel_launch_count.restype = ctypes.c_uint64
+    L.msa_status_string.argtypes = [ci]
+    L.msa_status_string.restype = ctypes.c_char_p
+    for f in ("msa_index_topk", "msa_sparse_attn", "msa_forward", "msa_workspace_status"):
+        getattr(L, f).restype = ci
+    if path == _build.LIBMSA:
+        _lib = L
+    return L
+
+
+def msa_status_string(status):
+    return load().msa_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(getattr(stream, "cuda_stream", stream))
+
+
+def _host_i32(x, B):
+    vals = [int(v) for v in (x if hasattr(x, "__len__") else [x] * B)]
+    if len(vals) != B:
+        raise ValueError("expected %d positions, got %d" % (B, len(vals)))
+    return (ctypes.c_int32 * B)(*vals)
+
+
+def msa_kernel_launch_count():
+    return int(load().msa_kernel_launch_count())
+
+
+def msa_workspace_bytes(p):
+    return int(load().msa_workspace_bytes(ctypes.byref(p)))
+
+
+def workspace(p, device="cuda"):
+    """A device scratch buffer of msa_workspace_bytes(p) bytes."""
+    import torch
+    n = msa_workspace_bytes(p)
+    if n == 0:
+        raise MsaError(-2, "msa_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _call(rc, what):
+    if rc != 0:
+        raise MsaError(rc, what)
+
+
+def msa_index_topk(p, q_idx, k_idx, q_start, kv_len, sel, ws, stream=None):
+    _call(load().msa_index_topk(ctypes.byref(p), _ptr(q_idx), _ptr(k_idx),
+                                _host_i32(q_start, p.B), _host_i32(kv_len, p.B), _ptr(sel),
+                                _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+          "msa_index_topk")
+
+
+def msa_sparse_attn(p, q, k_cache, v_cache, sel, q_start, kv_len, out, ws, stream=None):
+    _call(load().msa_sparse_attn(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(sel), _host_i32(q_start, p.B), _host_i32(kv_len, p.B),
+                                 _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+                                 _stream(stream)), "msa_sparse_attn")
+
+
+def msa_forward(p, q_idx, k_idx, q, k_cache, v_cache, q_start, kv_len, out, ws, sel_out=None,
+                stream=None):
+    _call(load().msa_forward(ctypes.byref(p), _ptr(q_idx), _ptr(k_idx), _ptr(q), _ptr(k_cache),
+                             _ptr(v_cache), _host_i32(q_start, p.B), _host_i32(kv_len, p.B),
+                             _ptr(sel_out), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+                             _stream(stream)), "msa_forward")
+
+
+def msa_workspace_status(ws, stream=None):
+    """Waits for the stream; raises MsaError if a kernel recorded an error in ws."""
+    _call(load().msa_workspace_status(_ptr(ws), _stream(stream)), "kernel status")

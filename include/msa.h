@@ -124,12 +124,19 @@ int msa_forward(const msa_params *p, const uint16_t *q_idx, const uint16_t *k_id
                 uint16_t *out, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Waits for `stream`, then returns the status the last call on ws left in
- * it: MSA_OK, or MSA_ERR_TIMEOUT if a kernel's bounded wait ran out (its
- * outputs are then incomplete).  MSA_ERR_CUDA if the read itself fails. */
+ * it: MSA_OK; MSA_ERR_TIMEOUT if a kernel's bounded wait ran out (its
+ * outputs are then incomplete); MSA_ERR_INVALID_ARG if msa_sparse_attn met
+ * a selected id outside [0, lb] or beyond max_blocks (that id was skipped,
+ * never read).  MSA_ERR_CUDA if the read itself fails. */
 int msa_workspace_status(const void *ws, cudaStream_t stream);
 
 /* A static, human-readable name of a status code. */
 const char *msa_status_string(int status);
+
+/* Diagnostics: the number of kernels this library has enqueued since it was
+ * loaded (all threads, all devices).  Benchmarks read it before and after a
+ * timed region to count the launches inside it. */
+uint64_t msa_kernel_launch_count(void);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,148 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/msa.h declares, and rejects bad arguments on the host before any CUDA
+call (a T == 0 call with valid arguments returns MSA_OK without touching CUDA).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_sparse_attention_04_gb300 as msa
+from block_sparse_attention_04_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, -1, -2, -3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return msa.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "msa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(msa_\w+)\s*\(", text, re.M)))
+
+
+def exported(path):
+    import subprocess
+    out = subprocess.check_output(["nm", "-D", "--defined-only", path]).decode()
+    return {l.split()[-1] for l in out.splitlines() if " T " in l}
+
+
+def test_exports_every_header_function(lib):
+    decl = header_functions()
+    assert set(decl) >= {"msa_index_topk", "msa_sparse_attn", "msa_forward",
+                         "msa_workspace_bytes", "msa_workspace_status", "msa_status_string"}
+    syms = exported(_build.LIBMSA)
+    missing = [f for f in decl if f not in syms]
+    assert not missing, missing
+    for f in decl:
+        assert hasattr(lib, f)
+
+
+def test_status_strings(lib):
+    for code, text in [(0, "ok"), (-1, "invalid argument"), (-2, "unsupported shape"),
+                       (-3, "workspace too small"), (-4, "CUDA error"),
+                       (-5, "kernel wait timed out")]:
+        assert msa.msa_status_string(code) == text
+    assert msa.msa_status_string(7) == "unknown status"
+
+
+def P(**kw):
+    base = dict(B=1, T=0, H=48, G=8, D=128, Di=64, max_blocks=256)
+    base.update(kw)
+    return msa.params(**base)
+
+
+def test_workspace_bytes(lib):
+    assert msa.msa_workspace_bytes(P(T=128)) > 0
+    assert msa.msa_workspace_bytes(P(T=4096)) >= msa.msa_workspace_bytes(P(T=128))
+    assert msa.msa_workspace_bytes(P(H=47)) == 0        # H % G != 0
+    assert msa.msa_workspace_bytes(P(D=96)) == 0
+    assert lib.msa_workspace_bytes(None) == 0
+
+
+class Buf:
+    """A fake, 256-byte aligned address that is never dereferenced."""
+    def __init__(self, addr):
+        self.addr = addr
+
+    def data_ptr(self):
+        return self.addr
+
+
+def call_index(p, q_start=(0,), kv_len=None, q_idx=0x10000, k_idx=0x20000, sel=0x30000,
+               ws=0x40000, ws_bytes=None):
+    L = msa.load()
+    B = p.B
+    qs = (ctypes.c_int32 * B)(*(list(q_start) * B)[:B])
+    kl = (ctypes.c_int32 * B)(*([p.T] * B if kv_len is None else list(kv_len) * B)[:B])
+    nb = msa.msa_workspace_bytes(p) if ws_bytes is None else ws_bytes
+    return L.msa_index_topk(ctypes.byref(p), q_idx, k_idx, qs, kl, sel, ws, nb, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(), OK),
+    (dict(H=47), INVALID),
+    (dict(B=0), INVALID),
+    (dict(T=-1), INVALID),
+    (dict(B=257), UNSUPPORTED),
+    (dict(D=96), UNSUPPORTED),
+    (dict(Di=48), UNSUPPORTED),
+    (dict(G=16, H=32), UNSUPPORTED),
+    (dict(max_blocks=40000), UNSUPPORTED),
+])
+def test_host_validation_of_params(lib, kw, expect):
+    assert call_index(P(**kw)) == expect
+
+
+def test_host_validation_of_block_and_topk(lib):
+    p = P()
+    p.block = 64
+    assert call_index(p) == UNSUPPORTED
+    p = P()
+    p.topk = 8
+    assert call_index(p) == UNSUPPORTED
+    p = P()
+    p.scale = float("nan")
+    assert call_index(p) == INVALID
+    p = P()
+    p.kernels = 9
+    assert call_index(p) == INVALID
+
+
+def test_host_validation_of_positions_pointers_and_workspace(lib):
+    p = P(T=0, max_blocks=4)
+    assert call_index(p, q_start=(0,), kv_len=(4 * 128,)) == OK
+    assert call_index(p, q_start=(-1,), kv_len=(10,)) == INVALID
+    assert call_index(p, q_start=(0,), kv_len=(4 * 128 + 1,)) == INVALID     # beyond capacity
+    p1 = P(T=5, max_blocks=4)
+    assert call_index(p1, q_start=(10,), kv_len=(14,)) == INVALID            # q_start+T > kv_len
+    assert call_index(p, q_idx=None) == INVALID
+    assert call_index(p, sel=0x30004) == INVALID                             # misaligned
+    assert call_index(p, ws=0x40010) == INVALID                              # ws not 256-aligned
+    assert call_index(p, ws=None) == INVALID
+    assert call_index(p1, q_start=(0,), kv_len=(5,),
+                      ws_bytes=msa.msa_workspace_bytes(p1) - 1) == WORKSPACE
+    L = msa.load()
+    assert L.msa_index_topk(None, 1, 1, None, None, 1, 1, 1, None) == INVALID
+    assert L.msa_workspace_status(None, None) == INVALID
+
+
+def test_forward_and_attn_validate_pointers(lib):
+    L = msa.load()
+    p = P(T=0, max_blocks=4)
+    qs = (ctypes.c_int32 * 1)(0)
+    kl = (ctypes.c_int32 * 1)(0)
+    n = msa.msa_workspace_bytes(p)
+    a = 0x100000
+    assert L.msa_forward(ctypes.byref(p), a, a, a, a, a, qs, kl, None, a, a, n, None) == OK
+    assert L.msa_forward(ctypes.byref(p), a, a, a, a, None, qs, kl, None, a, a, n, None) == INVALID
+    assert L.msa_forward(ctypes.byref(p), a, a, a, a, a, qs, kl, a + 4, a, a, n, None) == INVALID
+    assert L.msa_sparse_attn(ctypes.byref(p), a, a, a, a, qs, kl, a, a, n, None) == OK
+    assert L.msa_sparse_attn(ctypes.byref(p), a, a, a, None, qs, kl, a, a, n, None) == INVALID
+    assert L.msa_sparse_attn(ctypes.byref(p), a, a, a, a, None, kl, a, a, n, None) == INVALID

@@ -1,0 +1,145 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Block selections must be bit-exact (index inputs lie on the 2^-3 grid, so
+fp32 sums are exact in any order); outputs within max-abs 2e-2 and mean-abs
+2e-3 of the oracle's double-precision result.
+"""
+import numpy as np
+import pytest
+
+import msa_synth as syn
+from tests.helpers import Workload, assert_close, assert_sel_equal, run_forward, bf16_to_f64
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = ["streaming"]
+
+
+@pytest.fixture(scope="module")
+def msa():
+    import torch
+    assert torch.cuda.is_available()
+    import block_sparse_attention_04_gb300 as m
+    m.load()
+    return m
+
+
+def test_device_generator_equals_numpy_generator():
+    import torch
+    import msa_synth.device as sd
+    B, H, G, D, Di, nb = 2, 6, 2, 64, 32, 5
+    dev = sd.make_inputs(B, H, G, D, Di, nb, ctx_len=nb * 128, seed=77, q_rows=(100, 300))
+    for b in range(B):
+        assert np.array_equal(dev["k_idx"][b].cpu().numpy().view(np.uint16),
+                              syn.kidx_seq(77, b, nb * 128, Di))
+        assert np.array_equal(dev["k"][b].cpu().numpy().view(np.uint16),
+                              syn.kv_cache(77, syn.TID_K, b, nb, G, D))
+        assert np.array_equal(dev["v"][b].cpu().numpy().view(np.uint16),
+                              syn.kv_cache(77, syn.TID_V, b, nb, G, D))
+        assert np.array_equal(dev["q"][b].cpu().numpy().view(np.uint16),
+                              syn.q_rows(77, b, 100, 300, H, D))
+        assert np.array_equal(dev["q_idx"][b].cpu().numpy().view(np.uint16),
+                              syn.qidx_rows(77, b, 100, 300, G, Di))
+
+
+@pytest.mark.parametrize("kernels", KERNELS)
+@pytest.mark.parametrize("split", [False, True])
+def test_tiny_prefill_3072(msa, ref, kernels, split):
+    # 24 blocks of 128, 1 group of 4 heads, D 64, Di 32, every row checked
+    wl = Workload(B=1, T=3072, H=4, G=1, D=64, Di=32, ctx=[3072], q_start=[0])
+    want_sel, want_out = wl.oracle(ref)
+    sel, out = run_forward(msa, wl, kernels, split=split)
+    assert_sel_equal(sel, want_sel)
+    assert_close(out, want_out)
+
+
+@pytest.mark.parametrize("kernels", KERNELS)
+def test_prefill_m2_layout_ragged_tail(msa, ref, kernels):
+    # 48 query / 8 KV heads, D 128, Di 64; T not a multiple of the block
+    wl = Workload(B=1, T=2500, H=48, G=8, D=128, Di=64, ctx=[2500], q_start=[0])
+    want_sel, want_out = wl.oracle(ref)
+    sel, out = run_forward(msa, wl, kernels)
+    assert_sel_equal(sel, want_sel)
+    assert_close(out, want_out)
+
+
+@pytest.mark.parametrize("kernels", KERNELS)
+def test_chunked_prefill_matches_whole(msa, ref, kernels):
+    L = 2944
+    whole = Workload(B=1, T=L, H=12, G=2, D=128, Di=64, ctx=[L], q_start=[0])
+    want_sel, want_out = whole.oracle(ref)
+    for c0, c1 in [(0, 1024), (1024, 2048), (2048, 2900), (2900, 2944)]:
+        wl = Workload(B=1, T=c1 - c0, H=12, G=2, D=128, Di=64, ctx=[L], q_start=[c0],
+                      max_blocks=whole.max_blocks)
+        sel, out = run_forward(msa, wl, kernels)
+        assert_sel_equal(sel[0], want_sel[0, c0:c1])
+        assert_close(out[0], want_out[0, c0:c1])
+
+
+@pytest.mark.parametrize("kernels", KERNELS)
+def test_decode_batch_ragged_contexts(msa, ref, kernels):
+    ctx = [1, 127, 128, 129, 2048, 2049, 5000, 9000]
+    B = len(ctx)
+    wl = Workload(B=B, T=1, H=48, G=8, D=128, Di=64, ctx=ctx, q_start=[c - 1 for c in ctx],
+                  max_blocks=72)
+    want_sel, want_out = wl.oracle(ref)
+    sel, out = run_forward(msa, wl, kernels)
+    assert_sel_equal(sel, want_sel)
+    assert_close(out, want_out)
+    for b, c in enumerate(ctx):   # invariants: min(16, lb+1) ids, local block in
+        lb = (c - 1) // 128
+        for g in range(8):
+            ids = [x for x in sel[b, 0, g] if x >= 0]
+            assert len(ids) == min(16, lb + 1) and lb in ids and ids == sorted(ids)
+
+
+def test_sparse_attn_with_caller_selection(msa, ref):
+    import torch
+    wl = Workload(B=2, T=300, H=8, G=2, D=64, Di=32, ctx=[4000, 4000], q_start=[3700, 3000],
+                  max_blocks=32)
+    rng = np.random.default_rng(1)
+    sel = np.full((2, 300, 2, 16), -1, np.int32)
+    for b in range(2):
+        for i in range(300):
+            lb = (wl.q_start[b] + i) // 128
+            for g in range(2):
+                n = rng.integers(1, 17)
+                ids = rng.choice(lb + 1, size=min(n, lb + 1), replace=False)
+                slots = rng.choice(16, size=len(ids), replace=False)
+                sel[b, i, g, slots] = ids                  # unsorted, with -1 holes
+    d = wl.dims(ref)
+    want = ref.sparse_attn(d, wl.q, wl.k, wl.v, sel, np.array(wl.q_start, np.int32),
+                           np.array(wl.kv_len, np.int32), wl.max_blocks)
+    dev = wl.device()
+    p = wl.params(msa, "streaming")
+    ws = msa.workspace(p)
+    out = torch.full((2, 300, 8, 64), 0x7FC0, dtype=torch.int16, device="cuda")
+    msa.msa_sparse_attn(p, dev["q"], dev["k"], dev["v"], torch.from_numpy(sel).cuda(),
+                        wl.q_start, wl.kv_len, out, ws)
+    msa.msa_workspace_status(ws)
+    assert_close(bf16_to_f64(out.cpu().numpy()), want)
+
+
+def test_out_of_range_selection_is_reported_not_read(msa):
+    import torch
+    wl = Workload(B=1, T=4, H=4, G=1, D=64, Di=32, ctx=[600], q_start=[500], max_blocks=5)
+    dev = wl.device()
+    p = wl.params(msa, "streaming")
+    ws = msa.workspace(p)
+    sel = torch.full((1, 4, 1, 16), -1, dtype=torch.int32, device="cuda")
+    sel[0, :, 0, 0] = 3
+    sel[0, 0, 0, 1] = 4          # the block after query 500's local block 3
+    out = torch.empty((1, 4, 4, 64), dtype=torch.int16, device="cuda")
+    msa.msa_sparse_attn(p, dev["q"], dev["k"], dev["v"], sel, wl.q_start, wl.kv_len, out, ws)
+    with pytest.raises(msa.MsaError) as e:
+        msa.msa_workspace_status(ws)
+    assert e.value.status == -1
+
+
+def test_zero_length_call_is_a_noop(msa):
+    import torch
+    p = msa.params(2, 0, 4, 1, 64, 32, 4)
+    ws = msa.workspace(p)
+    z = torch.zeros(16, dtype=torch.int16, device="cuda")
+    msa.msa_forward(p, z, z, z, z, z, [0, 5], [0, 5], z, ws)
+    torch.cuda.synchronize()

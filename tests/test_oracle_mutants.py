@@ -22,9 +22,9 @@ MUTANTS = {
     "min_pool": ("if (s > best) best = s;", "if (best == -INFINITY || s < best) best = s;"),
     # sum pooling instead of max pooling
     "sum_pool": ("if (s > best) best = s;", "best = (best == -INFINITY ? 0.0 : best) + s;"),
-    # local block counted on top of the topk (17 instead of 16)
-    "local_extra": ("int64_t nsel = lb + 1 < p->topk ? lb + 1 : p->topk;",
-                    "int64_t nsel = lb + 1 < p->topk + 1 ? lb + 1 : p->topk + 1;"),
+    # plain top-16 of the candidates: the local block is not forced in
+    "local_not_forced": ("s[0] = (int32_t)lb;",
+                         "s[0] = lb >= p->topk ? cand[p->topk - 1].blk : (int32_t)lb;"),
     # causal clip of the local block dropped
     "no_causal_clip": ("if (tok > t) continue;", "(void)0;"),
     # softmax scale dropped
