@@ -14,14 +14,15 @@ from . import _build
 
 __all__ = ["MsaParams", "MsaError", "params", "load", "msa_workspace_bytes", "msa_index_topk",
            "msa_sparse_attn", "msa_forward", "msa_workspace_status", "msa_status_string",
-           "msa_kernel_launch_count",
+           "msa_kernel_launch_count", "msa_index_topk_noalloc",
            "workspace", "BLOCK", "TOPK"]
 
 BLOCK = 128
 TOPK = 16
 KERNELS = {"auto": 0, "streaming": 1, "tensorcore": 2}
 EXPORTS = ("msa_workspace_bytes", "msa_index_topk", "msa_sparse_attn", "msa_forward",
-           "msa_workspace_status", "msa_status_string", "msa_kernel_launch_count")
+           "msa_workspace_status", "msa_status_string", "msa_kernel_launch_count",
+           "msa_index_topk_noalloc")
 
 
 class MsaError(RuntimeError):
@@ -63,11 +64,13 @@ def load(path=None):
     L.msa_sparse_attn.argtypes = [PP, P, P, P, P, P, P, P, P, sz, P]
     L.msa_forward.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, sz, P]
     L.msa_workspace_status.argtypes = [P, P]
+    L.msa_index_topk_noalloc.argtypes = [PP, P, P, P, P, P, P]
     L.msa_kernel_launch_count.argtypes = []
     L.msa_kernel_launch_count.restype = ctypes.c_uint64
     L.msa_status_string.argtypes = [ci]
     L.msa_status_string.restype = ctypes.c_char_p
-    for f in ("msa_index_topk", "msa_sparse_attn", "msa_forward", "msa_workspace_status"):
+    for f in ("msa_index_topk", "msa_sparse_attn", "msa_forward", "msa_workspace_status",
+              "msa_index_topk_noalloc"):
         getattr(L, f).restype = ci
     if path == _build.LIBMSA:
         _lib = L
@@ -127,6 +130,14 @@ def msa_index_topk(p, q_idx, k_idx, q_start, kv_len, sel, ws, stream=None):
                                 _host_i32(q_start, p.B), _host_i32(kv_len, p.B), _ptr(sel),
                                 _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
           "msa_index_topk")
+
+
+def msa_index_topk_noalloc(p, q_idx, k_idx, q_start, kv_len, sel, stream=None):
+    """msa_index_topk without a workspace: for callers that cannot allocate
+    device memory (scratch lives in a static array inside the library)."""
+    _call(load().msa_index_topk_noalloc(ctypes.byref(p), _ptr(q_idx), _ptr(k_idx),
+                                        _host_i32(q_start, p.B), _host_i32(kv_len, p.B),
+                                        _ptr(sel), _stream(stream)), "msa_index_topk_noalloc")
 
 
 def msa_sparse_attn(p, q, k_cache, v_cache, sel, q_start, kv_len, out, ws, stream=None):

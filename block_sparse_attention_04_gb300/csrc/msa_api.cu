@@ -14,16 +14,8 @@ namespace msa {
 static std::atomic<uint64_t> g_launches{0};
 void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
-namespace {
-
-constexpr size_t kAlign = 256;
-constexpr int kStreamRows = 2048;   // query rows per streaming pass
 constexpr int kMaxContextBlocks = 32768;
 constexpr bool kHaveTensorcore = false;
-
-size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
-
-bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 int validate_params(const msa_params* p) {
   if (!p) return MSA_ERR_INVALID_ARG;
@@ -61,6 +53,16 @@ int validate_positions(const msa_params* p, const int32_t* q_start, const int32_
 Shape shape_of(const msa_params* p) {
   return Shape{p->B, p->T, p->H, p->G, p->D, p->Di, p->max_blocks, p->scale};
 }
+
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kStreamRows = 2048;   // query rows per streaming pass
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 bool use_tensorcore(const msa_params* p) {
   if (p->kernels == MSA_KERNELS_TENSORCORE) return true;

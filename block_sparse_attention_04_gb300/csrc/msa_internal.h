@@ -48,6 +48,12 @@ struct Workspace {
   size_t tc_bytes;
 };
 
+// Host-side argument checks shared by every entry point (MSA_OK or a status).
+int validate_params(const msa_params* p);
+int validate_positions(const msa_params* p, const int32_t* q_start, const int32_t* kv_len,
+                       Positions* pos);
+Shape shape_of(const msa_params* p);
+
 // ---- streaming kernels (any shape; the decode path) -----------------------
 // Rows of a pass are queries [t0, t1) of every sequence.
 cudaError_t launch_index_stream(const Shape& s, const Positions& pos, int t0, int t1,

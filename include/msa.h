@@ -63,6 +63,7 @@ extern "C" {
 #define MSA_BLOCK 128
 #define MSA_TOPK 16
 #define MSA_MAX_BATCH 256
+#define MSA_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 typedef enum {
   MSA_OK = 0,
@@ -122,6 +123,34 @@ int msa_forward(const msa_params *p, const uint16_t *q_idx, const uint16_t *k_id
                 const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                 const int32_t *q_start, const int32_t *kv_len, int32_t *sel_out,
                 uint16_t *out, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* msa_index_topk for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a deployment variant of steps 1-3, not part
+ * of the method.
+ *
+ * Some callers cannot call cudaMalloc: a serving engine that gives all free
+ * GPU memory to its KV-cache pool at start-up and forbids later allocations,
+ * or a plugin host that passes the library nothing but its input and output
+ * buffers.  Such callers cannot supply the workspace msa_index_topk takes.
+ * This entry point takes none and allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library call): its scratch is a static device
+ * array of MSA_NOALLOC_SCRATCH_BYTES bytes inside the library, which every
+ * GPU that loads the library holds until the process exits.
+ *   - Same arguments and results as msa_index_topk (sel is bit-identical),
+ *     minus ws/ws_bytes.  The stream must belong to the current device.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Returns MSA_ERR_WORKSPACE when the call would need more scratch than
+ *     MSA_NOALLOC_SCRATCH_BYTES (B*T*ceil(max lb/64)*G*15*8 bytes, splits
+ *     capped at 128), MSA_ERR_UNSUPPORTED when B*T > 65535.
+ *   - Every call shares the one array and leaves its contents behind; each
+ *     call writes every scratch entry it reads, so nothing needs clearing.
+ *     Calls that overlap on the GPU (other streams, other host threads) race
+ *     on the array: the caller must serialise them. */
+int msa_index_topk_noalloc(const msa_params *p, const uint16_t *q_idx, const uint16_t *k_idx,
+                           const int32_t *q_start, const int32_t *kv_len, int32_t *sel,
+                           cudaStream_t stream);
 
 /* Waits for `stream`, then returns the status the last call on ws left in
  * it: MSA_OK; MSA_ERR_TIMEOUT if a kernel's bounded wait ran out (its
