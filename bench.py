@@ -10,6 +10,7 @@ synthetic inputs already resident in HBM:
   prefill_128k  one 131072-token sequence, one call
   prefill_1m    one 1,048,576-token sequence, 128 chunked calls of 8192 queries
   prefill_32k   one 32768-token sequence
+  decode_small  8 x 131072 decode (a small case for profiler captures)
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle (the
 reference arm) on a bounded sample of the same workload instead.
@@ -34,6 +35,8 @@ WORKLOADS = {
     "prefill_128k": dict(cfg=2, kind="prefill", B=1, L=131072, chunk=131072),
     "decode_256k": dict(cfg=3, kind="decode", B=64, L=262144),
     "prefill_1m": dict(cfg=4, kind="prefill", B=1, L=1048576, chunk=8192),
+    # profiling case: decode shapes at 8 x 131072 (K_idx 134 MB > L2, ~4 GB on device)
+    "decode_small": dict(cfg=3, kind="decode", B=8, L=131072),
 }
 DEFAULT_WORKLOAD = "decode_256k"
 
