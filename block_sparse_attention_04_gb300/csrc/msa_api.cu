@@ -15,7 +15,6 @@ static std::atomic<uint64_t> g_launches{0};
 void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 constexpr int kMaxContextBlocks = 32768;
-constexpr bool kHaveTensorcore = false;
 
 int validate_params(const msa_params* p) {
   if (!p) return MSA_ERR_INVALID_ARG;
@@ -31,7 +30,10 @@ int validate_params(const msa_params* p) {
   if (p->Di != 32 && p->Di != 64) return MSA_ERR_UNSUPPORTED;
   if (p->G > 8 || p->H / p->G > 16) return MSA_ERR_UNSUPPORTED;
   if (p->max_blocks > kMaxContextBlocks) return MSA_ERR_UNSUPPORTED;
-  if (p->kernels == MSA_KERNELS_TENSORCORE && !kHaveTensorcore) return MSA_ERR_UNSUPPORTED;
+  // TMA coordinates are 32-bit: rows of q_idx and of k_idx must fit
+  if ((int64_t)p->B * p->T * p->G >= ((int64_t)1 << 31) ||
+      (int64_t)p->B * p->max_blocks * MSA_BLOCK >= ((int64_t)1 << 31))
+    return MSA_ERR_UNSUPPORTED;
   return MSA_OK;
 }
 
@@ -64,11 +66,16 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-bool use_tensorcore(const msa_params* p) {
+// Index scan on tensor cores for prefill-sized calls (>= 256 query-group rows
+// per sequence fill one work item), streaming otherwise.
+bool use_tc_index(const msa_params* p) {
   if (p->kernels == MSA_KERNELS_TENSORCORE) return true;
   if (p->kernels == MSA_KERNELS_STREAMING) return false;
-  return kHaveTensorcore && (int64_t)p->T * p->G >= 256;  // prefill-sized
+  return (int64_t)p->T * p->G >= 256;
 }
+
+// KV-outer tensor-core attention for prefill-sized calls.
+bool use_tc_attn(const msa_params* p) { return use_tc_index(p); }
 
 int stream_pass_len(const msa_params* p) {
   int tc = kStreamRows / p->B;
@@ -78,27 +85,29 @@ int stream_pass_len(const msa_params* p) {
 
 struct Plan {
   size_t status_off, sel_off, scratch_off, total;
-  size_t cand_entries, part_rows, csr_words, tc_bytes;
+  size_t cand_entries, part_rows;
 };
 
 Plan plan_for(const msa_params* p) {
   Plan pl{};
   const Shape s = shape_of(p);
   const int max_lb = p->max_blocks - 1;
-  const bool tc = use_tensorcore(p);
-  size_t scratch = 0;
-  if (!tc) {
-    const int rows = p->B * stream_pass_len(p);
-    pl.cand_entries = index_stream_cand_entries(s, rows, max_lb);
-    pl.part_rows = attn_stream_part_rows(s, rows);
-    const size_t idx = align_up(pl.cand_entries * sizeof(Cand));
-    const size_t att = align_up(pl.part_rows * p->D * sizeof(float)) +
-                       align_up(pl.part_rows * 2 * sizeof(float));
-    scratch = idx > att ? idx : att;
+  const int rows = p->B * stream_pass_len(p);
+  size_t idx = 0, att = 0;
+  if (use_tc_index(p)) {
+    idx = align_up(tc_index_workspace_bytes(s));
+    pl.cand_entries = idx / sizeof(Cand);
   } else {
-    pl.tc_bytes = tc_workspace_bytes(s);
-    scratch = pl.tc_bytes;
+    pl.cand_entries = index_stream_cand_entries(s, rows, max_lb);
+    idx = align_up(pl.cand_entries * sizeof(Cand));
   }
+  if (use_tc_attn(p)) {
+    att = align_up(tc_attn_workspace_bytes(s));
+  } else {
+    pl.part_rows = attn_stream_part_rows(s, rows);
+    att = align_up(pl.part_rows * p->D * sizeof(float)) + align_up(pl.part_rows * 2 * sizeof(float));
+  }
+  const size_t scratch = idx > att ? idx : att;
   pl.status_off = 0;
   pl.sel_off = kAlign;
   pl.scratch_off = pl.sel_off + align_up((size_t)p->B * p->T * p->G * MSA_TOPK * sizeof(int32_t));
@@ -118,7 +127,7 @@ Workspace carve(const msa_params* p, const Plan& pl, void* ws) {
   w.part_rows = pl.part_rows;
   w.part_ml = reinterpret_cast<float*>(scr + align_up(pl.part_rows * p->D * sizeof(float)));
   w.tc_base = scr;
-  w.tc_bytes = pl.tc_bytes;
+  w.tc_bytes = pl.total - pl.scratch_off;
   return w;
 }
 
@@ -134,7 +143,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA
 int run_index(const msa_params* p, const Positions& pos, const uint16_t* q_idx,
               const uint16_t* k_idx, int32_t* sel, const Workspace& w, cudaStream_t st) {
   const Shape s = shape_of(p);
-  if (use_tensorcore(p)) return cuda_status(launch_index_tc(s, pos, q_idx, k_idx, sel, w, st));
+  if (use_tc_index(p)) return cuda_status(launch_index_tc(s, pos, q_idx, k_idx, sel, w, st));
   const int tc = stream_pass_len(p);
   for (int t0 = 0; t0 < p->T; t0 += tc) {
     const int t1 = t0 + tc < p->T ? t0 + tc : p->T;
@@ -148,7 +157,7 @@ int run_attn(const msa_params* p, const Positions& pos, const uint16_t* q, const
              const uint16_t* v, const int32_t* sel, uint16_t* out, const Workspace& w,
              cudaStream_t st) {
   const Shape s = shape_of(p);
-  if (use_tensorcore(p)) return cuda_status(launch_attn_tc(s, pos, q, k, v, sel, out, w, st));
+  if (use_tc_attn(p)) return cuda_status(launch_attn_tc(s, pos, q, k, v, sel, out, w, st));
   const int tc = stream_pass_len(p);
   for (int t0 = 0; t0 < p->T; t0 += tc) {
     const int t1 = t0 + tc < p->T ? t0 + tc : p->T;

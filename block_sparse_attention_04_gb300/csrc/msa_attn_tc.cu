@@ -1,0 +1,530 @@
+// KV-outer sparse attention on tensor cores (prefill): step 4 of "MiniMax
+// 模型迭代与竞品分析" section 2 (exact softmax over the selected blocks only),
+// organised around the KV blocks, the "KV-outer" order that "MiniMax：Text-01 /
+// M1 → M2.7 → M3" section 5 names for MSA's sparse kernel.
+//
+// A query-outer tile would hold one query's heads of one group (6 rows),
+// far below the 128 rows a tcgen05 MMA wants.  So the selections are inverted:
+// for every (sequence b, KV block kb, group g) the (query, slot) entries that
+// chose it.  One tile = one such block x up to R = 128/(H/G) entries, i.e.
+// R*(H/G) <= 128 query-head rows against the block's 128 tokens:
+//   TMA           K and V of block kb, KV head g (block-major cache: 128 rows of
+//                 D bf16 at stride G*D)
+//   warps 0-3     gather the Q rows of the tile's entries into swizzled smem
+//   warp 8        tcgen05.mma  S = Q K^T (TMEM)  and  O = P V (TMEM, V MN-major)
+//   warps 4-7     row softmax of S (block-local max m, sum l; causal mask on the
+//                 local block), P as bf16 into smem, then O/l as a bf16 partial
+// Each (query, head, slot) partial (O/l, m, l) is combined by a log-sum-exp
+// merge into the bf16 output.
+#include <climits>
+
+#include "msa_device.cuh"
+#include "msa_tc.h"
+#include "msa_tma.h"
+
+namespace msa {
+namespace {
+
+constexpr int kAttnThreads = 288;  // 9 warps
+constexpr int kPassRows = 8192;    // (sequence, query) rows per pass
+
+struct AttnPass {
+  Shape s;
+  Positions pos;
+  int t0, Tp;            // queries [t0, t0+Tp) of every sequence
+  int nbl;               // key blocks per (sequence, group) in the list space
+  int nlists;            // B * nbl * G
+  int R;                 // entries per tile = 128 / (H/G)
+  const int32_t* sel;    // [B][T][G][16]
+  int32_t* count;        // [nlists]
+  int32_t* cursor;       // [nlists]
+  int32_t* off;          // [nlists + 1]   entry offsets
+  int32_t* tile_off;     // [nlists + 1]   tile offsets; tile_off[nlists] = total
+  int32_t* entries;      // packed (i - t0) * 16 + slot
+  int32_t* tile_list;    // list of each tile
+  uint16_t* part_o;      // [B*Tp*H*16][D] bf16, O / l
+  float2* part_ml;       // [B*Tp*H*16] (m in log2 units, l)
+  int* status;
+};
+
+__device__ __forceinline__ bool slot_valid(const AttnPass& a, int b, int i, int kb) {
+  const int64_t t = (int64_t)a.pos.q_start[b] + i;
+  return kb >= 0 && kb <= (int)(t / kBlock) && kb < a.s.max_blocks;
+}
+
+// ---- inverted lists -------------------------------------------------------
+__global__ void csr_count_kernel(AttnPass a) {
+  const int64_t n = (int64_t)a.s.B * a.Tp * a.s.G * kTopk;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int j = (int)(e % kTopk);
+    const int64_t rg = e / kTopk;
+    const int g = (int)(rg % a.s.G);
+    const int64_t r = rg / a.s.G;
+    const int b = (int)(r / a.Tp), i = a.t0 + (int)(r % a.Tp);
+    const int kb = a.sel[(((size_t)b * a.s.T + i) * a.s.G + g) * kTopk + j];
+    if (kb < 0) continue;
+    if (!slot_valid(a, b, i, kb)) {
+      atomicExch(a.status, 2);
+      continue;
+    }
+    atomicAdd(&a.count[((size_t)b * a.nbl + kb) * a.s.G + g], 1);
+  }
+}
+
+// Exclusive scans of entry counts and of tile counts, one CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) csr_scan_kernel(AttnPass a) {
+  __shared__ int64_t s_e[1024], s_t[1024];
+  const int n = a.nlists;
+  const int per = (n + 1023) / 1024;
+  const int lo = threadIdx.x * per, hi = min(n, lo + per);
+  int64_t se = 0, st = 0;
+  for (int k = lo; k < hi; ++k) {
+    const int c = a.count[k];
+    se += c;
+    st += (c + a.R - 1) / a.R;
+  }
+  s_e[threadIdx.x] = se;
+  s_t[threadIdx.x] = st;
+  __syncthreads();
+  for (int d = 1; d < 1024; d <<= 1) {
+    int64_t ve = 0, vt = 0;
+    if ((int)threadIdx.x >= d) {
+      ve = s_e[threadIdx.x - d];
+      vt = s_t[threadIdx.x - d];
+    }
+    __syncthreads();
+    s_e[threadIdx.x] += ve;
+    s_t[threadIdx.x] += vt;
+    __syncthreads();
+  }
+  int64_t oe = s_e[threadIdx.x] - se, ot = s_t[threadIdx.x] - st;
+  for (int k = lo; k < hi; ++k) {
+    const int c = a.count[k];
+    a.off[k] = (int32_t)oe;
+    a.tile_off[k] = (int32_t)ot;
+    oe += c;
+    ot += (c + a.R - 1) / a.R;
+  }
+  if (threadIdx.x == 1023) {
+    a.off[n] = (int32_t)s_e[1023];
+    a.tile_off[n] = (int32_t)s_t[1023];
+  }
+}
+
+__global__ void csr_fill_kernel(AttnPass a) {
+  const int64_t n = (int64_t)a.s.B * a.Tp * a.s.G * kTopk;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int j = (int)(e % kTopk);
+    const int64_t rg = e / kTopk;
+    const int g = (int)(rg % a.s.G);
+    const int64_t r = rg / a.s.G;
+    const int b = (int)(r / a.Tp), il = (int)(r % a.Tp);
+    const int kb = a.sel[(((size_t)b * a.s.T + a.t0 + il) * a.s.G + g) * kTopk + j];
+    if (!slot_valid(a, b, a.t0 + il, kb)) continue;
+    const int L = (b * a.nbl + kb) * a.s.G + g;
+    const int p = atomicAdd(&a.cursor[L], 1);
+    a.entries[a.off[L] + p] = il * kTopk + j;
+  }
+  // tile table: thread per list
+  for (int64_t L = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; L < a.nlists;
+       L += (int64_t)gridDim.x * blockDim.x) {
+    const int t0 = a.tile_off[L], t1 = a.tile_off[L + 1];
+    for (int k = t0; k < t1; ++k) a.tile_list[k] = (int32_t)L;
+  }
+}
+
+// ---- the attention tile kernel ---------------------------------------------
+template <int D>
+struct AttnCfg {
+  static constexpr int kHalf = 128 * 128;              // one [128 rows][64] bf16 SW128 box
+  static constexpr int kNHalf = D / 64;                // 64-dim halves of a row
+  static constexpr int kSmemQ = 2 * kHalf;             // Q tile, later P (128 x 128 tokens)
+  static constexpr int kSmemK = kNHalf * kHalf;
+  static constexpr int kSmemV = kNHalf * kHalf;
+  static constexpr int kSmem = kSmemQ + kSmemK + kSmemV + 256 + 1024;
+  static constexpr uint32_t kTmemCols = 256;            // S [0,128) and O [128, 128+D)
+};
+
+// Byte offset of 16-byte chunk `c` (0..7) of row `r` in a [128][64] bf16 box
+// with the 128-byte swizzle (chunk index XOR row mod 8).
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const uint16_t* __restrict__ q, const AttnPass a) {
+  using C = AttnCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sQ = smem;                       // Q, then P
+  uint8_t* sK = smem + C::kSmemQ;
+  uint8_t* sV = sK + C::kSmemK;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + C::kSmemV);
+  uint64_t* bar_kv = bars + 0;
+  uint64_t* bar_q = bars + 1;
+  uint64_t* bar_s = bars + 2;
+  uint64_t* bar_p = bars + 3;
+  uint64_t* bar_o = bars + 4;
+  uint64_t* bar_done = bars + 5;
+  uint64_t* bar_fin = bars + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(bar_kv, 1);
+    mbar_init(bar_q, 128);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_p, 128);
+    mbar_init(bar_o, 1);
+    mbar_init(bar_done, 128);
+    mbar_init(bar_fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 8) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int H = a.s.H, G = a.s.G, hpg = H / G;
+  const int ntiles = a.tile_off[a.nlists];
+  uint32_t it = 0;  // tiles processed by this CTA (barrier phase = it & 1)
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+    if (*abort_flag) break;
+    const uint32_t ph = it & 1;
+    const int L = a.tile_list[tile];
+    const int g = L % G;
+    const int kb = (L / G) % a.nbl;
+    const int b = L / (G * a.nbl);
+    const int e0 = (tile - a.tile_off[L]) * a.R;
+    const int ne = min(a.R, a.count[L] - e0);
+    const int32_t* ent = a.entries + a.off[L] + e0;
+    const int nrows = ne * hpg;
+
+    if (warp < 4) {
+      // -------------------------------------------------- loads (warps 0-3)
+      if (it > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_o, ph ^ 1, a.status))) { *abort_flag = 1; break; }
+      }
+      if (warp == 0 && lane == 0) {
+        mbar_arrive_expect_tx(bar_kv, 2 * C::kNHalf * C::kHalf);
+        const int row = (int)(((int64_t)b * a.s.max_blocks + kb) * kBlock);
+#pragma unroll
+        for (int h = 0; h < C::kNHalf; ++h) {
+          tma_load_3d(smem_u32(sK + h * C::kHalf), &tm_k, bar_kv, h * 64, g, row);
+          tma_load_3d(smem_u32(sV + h * C::kHalf), &tm_v, bar_kv, h * 64, g, row);
+        }
+      }
+      // Q rows: row r = entry e * hpg + head hh; 16-byte chunks, swizzled
+      const int tid = threadIdx.x;  // 0..127
+      constexpr int kChunks = D / 8;
+      for (int c = tid; c < nrows * kChunks; c += 128) {
+        const int r = c / kChunks, ch = c % kChunks;
+        const int e = r / hpg, hh = r - (r / hpg) * hpg;
+        const int il = ent[e] >> 4;
+        const uint16_t* src =
+            q + (((size_t)b * a.s.T + a.t0 + il) * H + (size_t)g * hpg + hh) * D + ch * 8;
+        cp_async_16(smem_u32(sQ + (ch >> 3) * C::kHalf + sw128(r, ch & 7)), src);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(bar_q);
+    } else if (warp == 8) {
+      // -------------------------------------------------- MMA (warp 8)
+      bool ok = true;
+      if (lane == 0) {
+        constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+        constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
+        ok = mbar_wait(bar_q, ph, a.status) && mbar_wait(bar_kv, ph, a.status) &&
+             (it == 0 || mbar_wait(bar_done, ph ^ 1, a.status));
+        if (ok) {
+          tc_fence_after();
+          const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * C::kHalf + (k & 3) * 32;
+            tc_mma_f16(tmem, smem_desc(q0 + off, 16, 1024, kSwizzle128B),
+                       smem_desc(k0 + off, 16, 1024, kSwizzle128B), idesc_s, k > 0);
+          }
+          tc_commit(bar_s);
+          ok = mbar_wait(bar_p, ph, a.status);
+          if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {  // 16 tokens per step
+              const uint32_t aoff = (k >> 2) * C::kHalf + (k & 3) * 32;
+              tc_mma_f16(tmem + 128, smem_desc(q0 + aoff, 16, 1024, kSwizzle128B),
+                         smem_desc(v0 + k * 2048, C::kHalf, 1024, kSwizzle128B), idesc_o, k > 0);
+            }
+            tc_commit(bar_o);
+          }
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { *abort_flag = 1; break; }
+    } else {
+      // -------------------------------------------------- softmax (warps 4-7)
+      const int quad = warp & 3;
+      const int r = quad * 32 + lane;  // tile row = TMEM lane
+      const bool valid = r < nrows;
+      int il = 0, hh = 0, slot = 0;
+      if (valid) {
+        const int e = r / hpg;
+        hh = r - e * hpg;
+        il = ent[e] >> 4;
+        slot = ent[e] & 15;
+      }
+      const int64_t t = (int64_t)a.pos.q_start[b] + a.t0 + il;
+      // tokens kb*128 + c with c > lim are masked (only in the local block)
+      const int lim = (int)(t - (int64_t)kb * kBlock);
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_s, ph, a.status))) { *abort_flag = 1; break; }
+      tc_fence_after();
+      const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+      uint32_t v[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + c * 32, v[c]);
+      tmem_ld_wait();
+      const float sl = a.s.scale * kLog2e;
+      float m = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float x = __uint_as_float(v[c][e]) * sl;
+          x = (c * 32 + e > lim) ? -INFINITY : x;
+          v[c][e] = __float_as_uint(x);
+          m = fmaxf(m, x);
+        }
+      float l = 0.f;
+      // P = 2^(s - m) as bf16, 16-byte chunks into the swizzled P tile (over Q)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e8 = 0; e8 < 4; ++e8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float p0 = ex2(__uint_as_float(v[c][e8 * 8 + 2 * u]) - m);
+            const float p1 = ex2(__uint_as_float(v[c][e8 * 8 + 2 * u + 1]) - m);
+            l += p0 + p1;
+            w[u] = pack_bf16(p0, p1);
+          }
+          const int chunk = c * 4 + e8;  // 8 tokens per chunk, 16 per row
+          const uint32_t addr =
+              smem_u32(sQ + (chunk >> 3) * C::kHalf + sw128(r, chunk & 7));
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                       "r"(w[2]), "r"(w[3])
+                       : "memory");
+        }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(bar_p);
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_o, ph, a.status))) { *abort_flag = 1; break; }
+      tc_fence_after();
+      uint32_t o[D / 32][32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + 128 + c * 32, o[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(bar_done);
+      if (valid) {
+        const size_t prow = (((size_t)b * a.Tp + il) * H + (size_t)g * hpg + hh) * kTopk + slot;
+        const float inv = 1.f / l;
+        uint16_t* dst = a.part_o + prow * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+          for (int e8 = 0; e8 < 4; ++e8) {
+            uint4 pk;
+            pk.x = pack_bf16(__uint_as_float(o[c][e8 * 8 + 0]) * inv, __uint_as_float(o[c][e8 * 8 + 1]) * inv);
+            pk.y = pack_bf16(__uint_as_float(o[c][e8 * 8 + 2]) * inv, __uint_as_float(o[c][e8 * 8 + 3]) * inv);
+            pk.z = pack_bf16(__uint_as_float(o[c][e8 * 8 + 4]) * inv, __uint_as_float(o[c][e8 * 8 + 5]) * inv);
+            pk.w = pack_bf16(__uint_as_float(o[c][e8 * 8 + 6]) * inv, __uint_as_float(o[c][e8 * 8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + c * 32 + e8 * 8) = pk;
+          }
+        a.part_ml[prow] = make_float2(m, l);
+      }
+    }
+  }
+
+  // all MMAs done before TMEM is released
+  if (warp == 8 && lane == 0) {
+    tc_commit(bar_fin);
+    mbar_wait(bar_fin, 0, nullptr);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---- merge: one warp per (sequence, query, head) ----------------------------
+template <int D>
+__global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnPass a, uint16_t* __restrict__ out) {
+  constexpr int PER = D / 32;
+  const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int H = a.s.H, hpg = H / a.s.G;
+  if (gw >= (int64_t)a.s.B * a.Tp * H) return;
+  const int h = (int)(gw % H);
+  const int64_t r = gw / H;
+  const int b = (int)(r / a.Tp), il = (int)(r % a.Tp);
+  const int i = a.t0 + il, g = h / hpg;
+  const size_t prow0 = (((size_t)b * a.Tp + il) * H + h) * kTopk;
+  float m = -INFINITY, l = 0.f;
+  if (lane < kTopk) {
+    const int kb = a.sel[(((size_t)b * a.s.T + i) * a.s.G + g) * kTopk + lane];
+    if (slot_valid(a, b, i, kb)) {
+      const float2 ml = a.part_ml[prow0 + lane];
+      m = ml.x;
+      l = ml.y;
+    }
+  }
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float w = (m == -INFINITY) ? 0.f : ex2(m - M) * l;
+  float W = w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  for (int j = 0; j < kTopk; ++j) {
+    const float wj = __shfl_sync(0xffffffffu, w, j);
+    if (wj == 0.f) continue;
+    const uint16_t* src = a.part_o + (prow0 + j) * D + lane * PER;
+    if constexpr (PER == 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(src);
+      acc[0] += wj * bf16lo(u.x);
+      acc[1] += wj * bf16hi(u.x);
+      acc[2] += wj * bf16lo(u.y);
+      acc[3] += wj * bf16hi(u.y);
+    } else {
+      const uint32_t u = *reinterpret_cast<const uint32_t*>(src);
+      acc[0] += wj * bf16lo(u);
+      acc[1] += wj * bf16hi(u);
+    }
+  }
+  const float inv = 1.f / W;
+  uint16_t* dst = out + (((size_t)b * a.s.T + i) * H + h) * D + lane * PER;
+#pragma unroll
+  for (int e = 0; e < PER; e += 2)
+    *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+}
+
+struct AttnLayout {
+  size_t lists, entries, count_off, cursor_off, off_off, toff_off, ent_off, tl_off, po_off, pml_off,
+      total;
+};
+
+AttnLayout attn_layout(const Shape& s) {
+  AttnLayout L{};
+  const int tp = pass_len(s);
+  L.lists = (size_t)s.B * s.max_blocks * s.G;
+  L.entries = (size_t)s.B * tp * s.G * kTopk;
+  auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  size_t o = 0;
+  L.count_off = o;  o += al(L.lists * 4);
+  L.cursor_off = o; o += al(L.lists * 4);
+  L.off_off = o;    o += al((L.lists + 1) * 4);
+  L.toff_off = o;   o += al((L.lists + 1) * 4);
+  L.ent_off = o;    o += al(L.entries * 4);
+  L.tl_off = o;     o += al(L.entries * 4);
+  const size_t prows = (size_t)s.B * tp * s.H * kTopk;
+  L.po_off = o;     o += al(prows * s.D * 2);
+  L.pml_off = o;    o += al(prows * 8);
+  L.total = o;
+  return L;
+}
+
+template <int D>
+cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint16_t* q,
+                                const uint16_t* k, const uint16_t* v, const int32_t* sel,
+                                uint16_t* out, const Workspace& ws, cudaStream_t st) {
+  using C = AttnCfg<D>;
+  const AttnLayout lay = attn_layout(s);
+  char* base = ws.tc_base;
+  CUtensorMap tm_k, tm_v;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)s.G,
+                          (cuuint64_t)s.B * s.max_blocks * kBlock};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)s.G * D * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)kBlock};
+    if (!encode_bf16_map(&tm_k, k, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_bf16_map(&tm_v, v, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_tc_kernel<D>, kAttnThreads, C::kSmem);
+  const int grid = sm_count() * (per_sm > 0 ? per_sm : 1);
+  const int tp_max = pass_len(s);
+  const int hpg = s.H / s.G;
+  for (int t0 = 0; t0 < s.T; t0 += tp_max) {
+    AttnPass a;
+    a.s = s;
+    a.pos = pos;
+    a.t0 = t0;
+    a.Tp = min(tp_max, s.T - t0);
+    const int max_lb = max_local_block(s, pos, t0, t0 + a.Tp);
+    a.nbl = max_lb + 1;
+    a.nlists = s.B * a.nbl * s.G;
+    a.R = 128 / hpg;
+    a.sel = sel;
+    a.count = reinterpret_cast<int32_t*>(base + lay.count_off);
+    a.cursor = reinterpret_cast<int32_t*>(base + lay.cursor_off);
+    a.off = reinterpret_cast<int32_t*>(base + lay.off_off);
+    a.tile_off = reinterpret_cast<int32_t*>(base + lay.toff_off);
+    a.entries = reinterpret_cast<int32_t*>(base + lay.ent_off);
+    a.tile_list = reinterpret_cast<int32_t*>(base + lay.tl_off);
+    a.part_o = reinterpret_cast<uint16_t*>(base + lay.po_off);
+    a.part_ml = reinterpret_cast<float2*>(base + lay.pml_off);
+    a.status = ws.status;
+    if ((e = cudaMemsetAsync(a.count, 0, (size_t)a.nlists * 4, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(a.cursor, 0, (size_t)a.nlists * 4, st)) != cudaSuccess) return e;
+    const int64_t n = (int64_t)s.B * a.Tp * s.G * kTopk;
+    const int g1 = (int)((n + 255) / 256 < 65536 ? (n + 255) / 256 : 65536);
+    note_launches(4);
+    csr_count_kernel<<<g1, 256, 0, st>>>(a);
+    csr_scan_kernel<<<1, 1024, 0, st>>>(a);
+    csr_fill_kernel<<<g1, 256, 0, st>>>(a);
+    attn_tc_kernel<D><<<grid, kAttnThreads, C::kSmem, st>>>(tm_k, tm_v, q, a);
+    const int64_t warps = (int64_t)s.B * a.Tp * s.H;
+    note_launches(1);
+    attn_tc_merge_kernel<D><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(a, out);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+int pass_len(const Shape& s) {
+  int tp = kPassRows / s.B;
+  if (tp < 1) tp = 1;
+  return tp < s.T ? tp : (s.T > 0 ? s.T : 1);
+}
+
+size_t tc_attn_workspace_bytes(const Shape& s) { return attn_layout(s).total; }
+
+cudaError_t launch_attn_tc(const Shape& s, const Positions& pos, const uint16_t* q,
+                           const uint16_t* k, const uint16_t* v, const int32_t* sel,
+                           uint16_t* out, const Workspace& ws, cudaStream_t st) {
+  if (s.D == 128) return launch_attn_tc_impl<128>(s, pos, q, k, v, sel, out, ws, st);
+  return launch_attn_tc_impl<64>(s, pos, q, k, v, sel, out, ws, st);
+}
+
+}  // namespace msa

@@ -101,16 +101,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: spins at most kWaitLimit polls.  On expiry it records
-// MSA_ERR_TIMEOUT in the status word and returns false; the caller then
-// stops issuing work and drains.
-constexpr uint32_t kWaitLimit = 1u << 26;
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: polls for at most kWaitNs of wall time.  On expiry it records
+// kDevTimeout in the status word (if given) and returns false; the caller then
+// stops issuing work and drains.  Every legitimate wait in these kernels lasts
+// microseconds.
+constexpr uint64_t kWaitNs = 2000000000ull;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitNs) {
+      if (status) atomicExch(status, (int)kDevTimeout);
+      return false;
+    }
   }
-  if (status) atomicExch(status, (int)kDevTimeout);
-  return false;
 }
 
 // --------------------------------------------------------------------- TMA --

@@ -160,33 +160,69 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(
   const int lb = (int)(t / kBlock);
   const int nvalid = (lb + bps - 1) / bps;
 
-  // lane owns splits lane, lane+32, lane+64, lane+96; cursors into each list
   const Cand* base = cand + (size_t)row * nsplit * s.G * kCand + (size_t)g * kCand;
-  int cur[4] = {0, 0, 0, 0};
+  const size_t lstride = (size_t)s.G * kCand;  // between the lists of consecutive splits
   int my_id = -1;
-  for (int r = 0; r < kCand; ++r) {
-    float bs = -INFINITY;
-    int bid = INT_MAX, bk = 0;
+  if (nvalid == 1) {
+    // one list: already the ranked top-15 of every candidate block
+    if (lane < kCand) {
+      const Cand c = base[lane];
+      my_id = (c.id == INT_MAX || lane >= lb) ? -1 : c.id;
+    }
+  } else if (nvalid <= 32) {
+    // lane l holds split l's sorted list in registers; the winner of each
+    // round shifts its list by one
+    float ls[kCand];
+    int li[kCand];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int sp = lane + 32 * k;
-      if (sp < nvalid && cur[k] < kCand) {
-        Cand c = base[(size_t)sp * s.G * kCand + cur[k]];
-        if (cand_better(c.score, c.id, bs, bid)) {
-          bs = c.score;
-          bid = c.id;
-          bk = k;
+    for (int k = 0; k < kCand; ++k) {
+      Cand c = Cand{-INFINITY, INT_MAX};
+      if (lane < nvalid) c = base[(size_t)lane * lstride + k];
+      ls[k] = c.score;
+      li[k] = c.id;
+    }
+    for (int r = 0; r < kCand; ++r) {
+      float bs = ls[0];
+      int bid = li[0], owner = lane;
+      warp_argbest(bs, bid, owner);
+      if (owner == lane) {
+#pragma unroll
+        for (int k = 0; k < kCand - 1; ++k) {
+          ls[k] = ls[k + 1];
+          li[k] = li[k + 1];
+        }
+        ls[kCand - 1] = -INFINITY;
+        li[kCand - 1] = INT_MAX;
+      }
+      if (lane == r) my_id = (bid == INT_MAX || r >= lb) ? -1 : bid;
+    }
+  } else {
+    // lane owns splits lane, lane+32, lane+64, lane+96; cursors into each list
+    int cur[4] = {0, 0, 0, 0};
+    for (int r = 0; r < kCand; ++r) {
+      float bs = -INFINITY;
+      int bid = INT_MAX, bk = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int sp = lane + 32 * k;
+        if (sp < nvalid && cur[k] < kCand) {
+          Cand c = base[(size_t)sp * lstride + cur[k]];
+          if (cand_better(c.score, c.id, bs, bid)) {
+            bs = c.score;
+            bid = c.id;
+            bk = k;
+          }
         }
       }
-    }
-    int owner = lane * 4 + bk;
-    warp_argbest(bs, bid, owner);
-    if ((owner >> 2) == lane) {
+      int owner = lane * 4 + bk;
+      warp_argbest(bs, bid, owner);
+      if ((owner >> 2) == lane) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (k == (owner & 3)) ++cur[k];
+        for (int k = 0; k < 4; ++k)
+          if (k == (owner & 3)) ++cur[k];
+      }
+      if (lane == r) my_id = (bid == INT_MAX || r >= lb) ? -1 : bid;
     }
-    if (lane == r) my_id = (bid == INT_MAX || r >= lb) ? -1 : bid;
   }
   if (lane == kCand) my_id = lb;
   // ascending order, -1 padding last
@@ -494,10 +530,18 @@ cudaError_t launch_index_stream(const Shape& s, const Positions& pos, int t0, in
       index_stream_kernel<32><<<grid, kIdxWarps * 32, 0, st>>>(s, pos, s.T, t0, Tp, bps, nsplit,
                                                                q_idx, k_idx, ws.cand);
   }
-  const int warps = rows * s.G;
+  return launch_topk_merge(s, pos, t0, t1, bps, nsplit > 0 ? nsplit : 1, ws.cand, sel, st);
+}
+
+cudaError_t launch_topk_merge(const Shape& s, const Positions& pos, int t0, int t1, int bps,
+                              int nsplit, const Cand* cand, int32_t* sel, cudaStream_t st) {
+  const int Tp = t1 - t0;
+  const int rows = s.B * Tp;
+  if (rows <= 0) return cudaSuccess;
+  const int64_t warps = (int64_t)rows * s.G;
   note_launches(1);
-  topk_merge_kernel<<<(warps + 7) / 8, 256, 0, st>>>(s, pos, s.T, t0, Tp, bps,
-                                                    nsplit > 0 ? nsplit : 1, rows, ws.cand, sel);
+  topk_merge_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(s, pos, s.T, t0, Tp, bps, nsplit,
+                                                               rows, cand, sel);
   return cudaGetLastError();
 }
 

@@ -4,15 +4,24 @@
 
 namespace msa {
 
-// Bytes of scratch the tensor-core index scan and KV-outer attention need.
-size_t tc_workspace_bytes(const Shape& s);
+// Scratch bytes of the tensor-core index scan: per-split candidate lists of
+// every (query, group) of the call.
+size_t tc_index_workspace_bytes(const Shape& s);
 
 // Steps 1-3 for every query of the call (tcgen05 index scan + merge).
 cudaError_t launch_index_tc(const Shape& s, const Positions& pos, const uint16_t* q_idx,
                             const uint16_t* k_idx, int32_t* sel, const Workspace& ws,
                             cudaStream_t st);
 
-// Step 4 for every query of the call (KV-outer tcgen05 attention + merge).
+// Queries per sequence in one pass of the tensor-core attention (the pass
+// bounds its scratch: at most 8192 (sequence, query) rows).
+int pass_len(const Shape& s);
+
+// Scratch bytes of the KV-outer attention for one pass.
+size_t tc_attn_workspace_bytes(const Shape& s);
+
+// Step 4 for every query of the call (inverted lists, KV-outer tcgen05
+// attention, log-sum-exp merge), in passes of pass_len(s) queries.
 cudaError_t launch_attn_tc(const Shape& s, const Positions& pos, const uint16_t* q,
                            const uint16_t* k, const uint16_t* v, const int32_t* sel,
                            uint16_t* out, const Workspace& ws, cudaStream_t st);

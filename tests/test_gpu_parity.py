@@ -12,7 +12,7 @@ from tests.helpers import Workload, assert_close, assert_sel_equal, run_forward,
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = ["streaming"]
+KERNELS = ["streaming", "tensorcore"]
 
 
 @pytest.fixture(scope="module")
@@ -93,7 +93,30 @@ def test_decode_batch_ragged_contexts(msa, ref, kernels):
             assert len(ids) == min(16, lb + 1) and lb in ids and ids == sorted(ids)
 
 
-def test_sparse_attn_with_caller_selection(msa, ref):
+@pytest.mark.parametrize("kernels", KERNELS)
+def test_unaligned_starts_in_several_sequences(msa, ref, kernels):
+    # rows of one work item straddle query blocks and sequences start mid-block
+    wl = Workload(B=3, T=700, H=12, G=4, D=64, Di=64, ctx=[700, 1033, 1700],
+                  q_start=[0, 333, 1000])
+    want_sel, want_out = wl.oracle(ref)
+    sel, out = run_forward(msa, wl, kernels)
+    assert_sel_equal(sel, want_sel)
+    assert_close(out, want_out)
+
+
+@pytest.mark.parametrize("kernels", KERNELS)
+def test_long_context_chunk_spans_several_splits(msa, ref, kernels):
+    # lb up to 312: the tensor-core scan splits the key range (256 blocks per split)
+    L = 40000
+    wl = Workload(B=1, T=1000, H=4, G=2, D=64, Di=64, ctx=[L], q_start=[L - 1000])
+    want_sel, want_out = wl.oracle(ref)
+    sel, out = run_forward(msa, wl, kernels)
+    assert_sel_equal(sel, want_sel)
+    assert_close(out, want_out)
+
+
+@pytest.mark.parametrize("kernels", KERNELS)
+def test_sparse_attn_with_caller_selection(msa, ref, kernels):
     import torch
     wl = Workload(B=2, T=300, H=8, G=2, D=64, Di=32, ctx=[4000, 4000], q_start=[3700, 3000],
                   max_blocks=32)
@@ -111,7 +134,7 @@ def test_sparse_attn_with_caller_selection(msa, ref):
     want = ref.sparse_attn(d, wl.q, wl.k, wl.v, sel, np.array(wl.q_start, np.int32),
                            np.array(wl.kv_len, np.int32), wl.max_blocks)
     dev = wl.device()
-    p = wl.params(msa, "streaming")
+    p = wl.params(msa, kernels)
     ws = msa.workspace(p)
     out = torch.full((2, 300, 8, 64), 0x7FC0, dtype=torch.int16, device="cuda")
     msa.msa_sparse_attn(p, dev["q"], dev["k"], dev["v"], torch.from_numpy(sel).cuda(),
@@ -120,11 +143,12 @@ def test_sparse_attn_with_caller_selection(msa, ref):
     assert_close(bf16_to_f64(out.cpu().numpy()), want)
 
 
-def test_out_of_range_selection_is_reported_not_read(msa):
+@pytest.mark.parametrize("kernels", KERNELS)
+def test_out_of_range_selection_is_reported_not_read(msa, kernels):
     import torch
     wl = Workload(B=1, T=4, H=4, G=1, D=64, Di=32, ctx=[600], q_start=[500], max_blocks=5)
     dev = wl.device()
-    p = wl.params(msa, "streaming")
+    p = wl.params(msa, kernels)
     ws = msa.workspace(p)
     sel = torch.full((1, 4, 1, 16), -1, dtype=torch.int32, device="cuda")
     sel[0, :, 0, 0] = 3
