@@ -3,7 +3,9 @@
 
 One step = the whole hot path (index scoring, block max-pooling, top-16 with
 the local block forced, sparse softmax attention) over one batch of seeded
-synthetic inputs already resident in HBM:
+synthetic inputs already resident in HBM.  The default line is the 1M-token
+chunked prefill, with the 64 x 256K decode batch measured in the same run and
+reported under "decode":
 
   decode_256k   64 sequences x 262144-token block-major caches, 1 new query
                 each (48 query / 8 KV heads, D 128, Di 64)
@@ -38,7 +40,8 @@ WORKLOADS = {
     # profiling case: decode shapes at 8 x 131072 (K_idx 134 MB > L2, ~4 GB on device)
     "decode_small": dict(cfg=3, kind="decode", B=8, L=131072),
 }
-DEFAULT_WORKLOAD = "decode_256k"
+DEFAULT_WORKLOAD = "prefill_1m"
+DEFAULT_SECONDARY = "decode_256k"
 
 
 # ------------------------------------------------------------ algorithmic work --
@@ -379,23 +382,23 @@ def reference_arm(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def gpu_arm(args, world, rank):
+def measure(name, args, world, rank):
+    """Time workload `name`; returns the fields of its JSON line."""
     import torch
-    import block_sparse_attention_04_gb300 as msa
-    msa.load()
     peaks, peak_kind = measured_peaks()
-    job = Job(args.workload, rank)
+    job = Job(name, rank)
     total_ms, idx_ms, att_ms, launches, clocks = time_job(job, args.steps, args.warmup, world)
     ms = total_ms / args.steps
     tokens = job.tokens() * world
-    value = tokens / (ms / 1000.0)
     w = job.w
     pos = job.positions()
     if w["kind"] == "decode":
         kidx_b, rest_b = decode_bytes(job.B, job.L)
-        roof = {"bound": "hbm", "kernel": "index scan (msa_index_topk: index_stream + topk_merge)",
+        roof = {"bound": "hbm",
+                "kernel": "index scan (msa_index_topk: index_stream + topk_merge)",
                 "achieved": kidx_b / (idx_ms / 1000.0) / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "traffic": None, "peak_kind": peak_kind}
+                "unit": "GB/s", "traffic": None, "peak_kind": peak_kind,
+                "bytes_per_launch": kidx_b}
         roof["frac"] = roof["achieved"] / roof["peak"]
         whole = {"bytes_per_step": kidx_b + rest_b,
                  "achieved_gbs": (kidx_b + rest_b) / (ms / 1000.0) / 1e9}
@@ -404,37 +407,57 @@ def gpu_arm(args, world, rank):
         fi = index_flops(pos) * job.B
         fa = attn_flops(pos) * job.B
         peak_tf = peaks["bf16_tflops_sustained"] if ms > 1000 else peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "kernel": "index scan (msa_index_topk)",
+        roof = {"bound": "tensor",
+                "kernel": "index scan (msa_index_topk: index_tc + topk_merge)",
                 "achieved": fi / (idx_ms / 1000.0) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
-                "traffic": None, "peak_kind": peak_kind}
+                "traffic": None, "peak_kind": peak_kind + (" sustained" if ms > 1000 else " burst"),
+                "flops_per_step": fi, "launches_per_step": len(job.calls)}
         roof["frac"] = roof["achieved"] / roof["peak"]
         whole = {"flops_per_step": fi + fa, "index_flops": fi, "attn_flops": fa,
                  "achieved_tflops": (fi + fa) / (ms / 1000.0) / 1e12,
                  "attn_achieved_tflops": fa / (att_ms / 1000.0) / 1e12}
         whole["frac_of_bf16_peak"] = whole["achieved_tflops"] / peak_tf
     e2e_ms, h2d, d2h = time_e2e(job, max(1, min(args.steps, 3)), world)
+    cfg = {"workload": name, "batch": job.B, "ctx": job.L, "calls_per_step": len(job.calls),
+           "queries_per_call": job.calls[0]["T"], "heads": H, "kv_heads": G, "head_dim": D,
+           "index_dim": DI, "block": BLK, "topk": 16, "l2": "inputs larger than L2 (no flush)"}
+    del job
+    torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        smp = OracleSample(args.workload)
+        smp = OracleSample(name)
         v, secs = smp.run()
         cpu = {"value": v, "unit": "tokens/s", "cores": smp.nthreads, "kind": "oracle",
                "sample": smp.desc, "seconds": secs}
+    return {"value": tokens / (ms / 1000.0), "ms_per_step": ms, "config": cfg, "roofline": roof,
+            "step": whole, "kernels_ms": {"index_topk": idx_ms, "sparse_attn": att_ms},
+            "e2e": {"value": tokens / (e2e_ms / 1000.0), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu}
+
+
+def gpu_arm(args, world, rank):
+    import block_sparse_attention_04_gb300 as msa
+    msa.load()
+    r = measure(args.workload, args, world, rank)
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded msa_synth generator: Irwin-Hall normals, 2^-3 index grid "
                 "with needles)",
-        "config": {"workload": args.workload, "batch": job.B, "ctx": job.L,
-                   "calls_per_step": len(job.calls), "queries_per_call": job.calls[0]["T"],
-                   "heads": H, "kv_heads": G, "head_dim": D, "index_dim": DI, "block": BLK,
-                   "topk": 16, "l2": "inputs larger than L2 (no flush)"},
-        "roofline": roof, "step": whole,
-        "kernels_ms": {"index_topk": idx_ms, "sparse_attn": att_ms},
-        "e2e": {"value": tokens / (e2e_ms / 1000.0), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
     }
+    for k in ("config", "roofline", "step", "kernels_ms", "e2e", "gpu_launches", "clocks",
+              "cpu_baseline"):
+        line[k] = r[k]
+    if args.secondary and args.secondary != args.workload:
+        s = measure(args.secondary, args, world, rank)
+        line[WORKLOADS[args.secondary]["kind"]] = {
+            "workload": args.secondary, "value": s["value"], "unit": "tokens/s",
+            "ms_per_step": s["ms_per_step"], "config": s["config"], "roofline": s["roofline"],
+            "step": s["step"], "kernels_ms": s["kernels_ms"], "e2e": s["e2e"],
+            "gpu_launches": s["gpu_launches"], "clocks": s["clocks"],
+            "cpu_baseline": s["cpu_baseline"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -448,8 +471,15 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--ref-rows", type=int, default=None,
                     help="rows of the bounded oracle sample per reference step")
+    ap.add_argument("--secondary", default=None,
+                    help="a second workload reported in the same line (default: decode_256k "
+                         "when the workload is the default one; 'none' to skip)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     args = ap.parse_args()
+    if args.secondary is None:
+        args.secondary = DEFAULT_SECONDARY if args.workload == DEFAULT_WORKLOAD else "none"
+    if args.secondary == "none":
+        args.secondary = None
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
         rank = int(os.environ.get("RANK", "0"))

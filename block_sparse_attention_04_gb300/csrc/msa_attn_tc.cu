@@ -154,7 +154,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(kAttnThreads, 2)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const uint16_t* __restrict__ q, const AttnPass a) {
   using C = AttnCfg<D>;
@@ -195,12 +195,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   const int H = a.s.H, G = a.s.G, hpg = H / G;
+  // a contiguous range of tiles per CTA: consecutive tiles of one list reuse
+  // the K/V block already in shared memory
   const int ntiles = a.tile_off[a.nlists];
-  uint32_t it = 0;  // tiles processed by this CTA (barrier phase = it & 1)
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+  const int per = (ntiles + gridDim.x - 1) / gridDim.x;
+  const int tile_lo = blockIdx.x * per;
+  const int tile_hi = min(ntiles, tile_lo + per);
+  uint32_t it = 0;      // tiles processed by this CTA (phase of the per-tile barriers)
+  uint32_t kv_it = 0;   // K/V loads issued by this CTA (phase of bar_kv)
+  int prev_list = -1;
+  for (int tile = tile_lo; tile < tile_hi; ++tile, ++it) {
     if (*abort_flag) break;
     const uint32_t ph = it & 1;
     const int L = a.tile_list[tile];
+    const bool reuse_kv = (L == prev_list);
+    prev_list = L;
+    const uint32_t kv_ph = reuse_kv ? ((kv_it - 1) & 1) : (kv_it & 1);
+    if (!reuse_kv) ++kv_it;
     const int g = L % G;
     const int kb = (L / G) % a.nbl;
     const int b = L / (G * a.nbl);
@@ -214,7 +225,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (it > 0) {
         if (!__all_sync(0xffffffffu, mbar_wait(bar_o, ph ^ 1, a.status))) { *abort_flag = 1; break; }
       }
-      if (warp == 0 && lane == 0) {
+      if (warp == 0 && lane == 0 && !reuse_kv) {
         mbar_arrive_expect_tx(bar_kv, 2 * C::kNHalf * C::kHalf);
         const int row = (int)(((int64_t)b * a.s.max_blocks + kb) * kBlock);
 #pragma unroll
@@ -224,9 +235,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
       // Q rows: row r = entry e * hpg + head hh; 16-byte chunks, swizzled
-      const int tid = threadIdx.x;  // 0..127
       constexpr int kChunks = D / 8;
-      for (int c = tid; c < nrows * kChunks; c += 128) {
+      for (int c = threadIdx.x; c < nrows * kChunks; c += 128) {
         const int r = c / kChunks, ch = c % kChunks;
         const int e = r / hpg, hh = r - (r / hpg) * hpg;
         const int il = ent[e] >> 4;
@@ -244,7 +254,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (lane == 0) {
         constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
         constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
-        ok = mbar_wait(bar_q, ph, a.status) && mbar_wait(bar_kv, ph, a.status) &&
+        ok = mbar_wait(bar_q, ph, a.status) && mbar_wait(bar_kv, kv_ph, a.status) &&
              (it == 0 || mbar_wait(bar_done, ph ^ 1, a.status));
         if (ok) {
           tc_fence_after();
@@ -288,70 +298,69 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(bar_s, ph, a.status))) { *abort_flag = 1; break; }
       tc_fence_after();
       const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-      uint32_t v[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + c * 32, v[c]);
-      tmem_ld_wait();
       const float sl = a.s.scale * kLog2e;
+      uint32_t v[32];
+      // pass 1: row max of the scaled, masked scores
       float m = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(lane_base + c * 32, v);
+        tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = __uint_as_float(v[c][e]) * sl;
-          x = (c * 32 + e > lim) ? -INFINITY : x;
-          v[c][e] = __float_as_uint(x);
-          m = fmaxf(m, x);
-        }
+        for (int e = 0; e < 32; ++e)
+          if (c * 32 + e <= lim) m = fmaxf(m, __uint_as_float(v[e]) * sl);
+      }
+      // pass 2: P = 2^(s - m) as bf16 into the swizzled P tile (over Q), row sum
       float l = 0.f;
-      // P = 2^(s - m) as bf16, 16-byte chunks into the swizzled P tile (over Q)
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(lane_base + c * 32, v);
+        tmem_ld_wait();
 #pragma unroll
         for (int e8 = 0; e8 < 4; ++e8) {
           uint32_t w[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const float p0 = ex2(__uint_as_float(v[c][e8 * 8 + 2 * u]) - m);
-            const float p1 = ex2(__uint_as_float(v[c][e8 * 8 + 2 * u + 1]) - m);
+            const int e = e8 * 8 + 2 * u;
+            const float p0 = (c * 32 + e <= lim) ? ex2(__uint_as_float(v[e]) * sl - m) : 0.f;
+            const float p1 = (c * 32 + e + 1 <= lim) ? ex2(__uint_as_float(v[e + 1]) * sl - m) : 0.f;
             l += p0 + p1;
             w[u] = pack_bf16(p0, p1);
           }
           const int chunk = c * 4 + e8;  // 8 tokens per chunk, 16 per row
-          const uint32_t addr =
-              smem_u32(sQ + (chunk >> 3) * C::kHalf + sw128(r, chunk & 7));
+          const uint32_t addr = smem_u32(sQ + (chunk >> 3) * C::kHalf + sw128(r, chunk & 7));
           asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
                        "r"(w[2]), "r"(w[3])
                        : "memory");
         }
+      }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       mbar_arrive(bar_p);
       if (!__all_sync(0xffffffffu, mbar_wait(bar_o, ph, a.status))) { *abort_flag = 1; break; }
       tc_fence_after();
-      uint32_t o[D / 32][32];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + 128 + c * 32, o[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(bar_done);
-      if (valid) {
-        const size_t prow = (((size_t)b * a.Tp + il) * H + (size_t)g * hpg + hh) * kTopk + slot;
-        const float inv = 1.f / l;
-        uint16_t* dst = a.part_o + prow * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c)
+      const float inv = 1.f / l;
+      const size_t prow = (((size_t)b * a.Tp + il) * H + (size_t)g * hpg + hh) * kTopk + slot;
+      uint16_t* dst = a.part_o + prow * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        tmem_ld32(lane_base + 128 + c * 32, v);
+        tmem_ld_wait();
+        if (valid) {
 #pragma unroll
           for (int e8 = 0; e8 < 4; ++e8) {
             uint4 pk;
-            pk.x = pack_bf16(__uint_as_float(o[c][e8 * 8 + 0]) * inv, __uint_as_float(o[c][e8 * 8 + 1]) * inv);
-            pk.y = pack_bf16(__uint_as_float(o[c][e8 * 8 + 2]) * inv, __uint_as_float(o[c][e8 * 8 + 3]) * inv);
-            pk.z = pack_bf16(__uint_as_float(o[c][e8 * 8 + 4]) * inv, __uint_as_float(o[c][e8 * 8 + 5]) * inv);
-            pk.w = pack_bf16(__uint_as_float(o[c][e8 * 8 + 6]) * inv, __uint_as_float(o[c][e8 * 8 + 7]) * inv);
+            pk.x = pack_bf16(__uint_as_float(v[e8 * 8 + 0]) * inv, __uint_as_float(v[e8 * 8 + 1]) * inv);
+            pk.y = pack_bf16(__uint_as_float(v[e8 * 8 + 2]) * inv, __uint_as_float(v[e8 * 8 + 3]) * inv);
+            pk.z = pack_bf16(__uint_as_float(v[e8 * 8 + 4]) * inv, __uint_as_float(v[e8 * 8 + 5]) * inv);
+            pk.w = pack_bf16(__uint_as_float(v[e8 * 8 + 6]) * inv, __uint_as_float(v[e8 * 8 + 7]) * inv);
             *reinterpret_cast<uint4*>(dst + c * 32 + e8 * 8) = pk;
           }
-        a.part_ml[prow] = make_float2(m, l);
+        }
       }
+      tc_fence_before();
+      mbar_arrive(bar_done);
+      if (valid) a.part_ml[prow] = make_float2(m, l);
     }
   }
 
