@@ -13,6 +13,7 @@ reported under "decode":
   prefill_1m    one 1,048,576-token sequence, 128 chunked calls of 8192 queries
   prefill_32k   one 32768-token sequence
   decode_small  8 x 131072 decode (a small case for profiler captures)
+  prefill_1m_last_chunk  the last 8192-query chunk of prefill_1m alone (profiling)
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle (the
 reference arm) on a bounded sample of the same workload instead.
@@ -37,8 +38,12 @@ WORKLOADS = {
     "prefill_128k": dict(cfg=2, kind="prefill", B=1, L=131072, chunk=131072),
     "decode_256k": dict(cfg=3, kind="decode", B=64, L=262144),
     "prefill_1m": dict(cfg=4, kind="prefill", B=1, L=1048576, chunk=8192),
-    # profiling case: decode shapes at 8 x 131072 (K_idx 134 MB > L2, ~4 GB on device)
+    # profiling cases (small enough for full profiler captures):
+    # decode shapes at 8 x 131072 (K_idx 134 MB > L2, ~4 GB on device), and the
+    # last 8192-query chunk of the 1M prefill alone (~4.5 GB on device)
     "decode_small": dict(cfg=3, kind="decode", B=8, L=131072),
+    "prefill_1m_last_chunk": dict(cfg=4, kind="prefill", B=1, L=1048576, chunk=8192,
+                                  only_last=True),
 }
 DEFAULT_WORKLOAD = "prefill_1m"
 DEFAULT_SECONDARY = "decode_256k"
@@ -178,9 +183,10 @@ class Job:
             qrows = (self.L - 1, self.L)
         else:
             c = w["chunk"]
-            self.calls = [dict(T=c, q_start=[s], kv_len=[s + c], qoff=s)
-                          for s in range(0, self.L, c)]
-            qrows = (0, self.L)
+            starts = [self.L - c] if w.get("only_last") else list(range(0, self.L, c))
+            self.calls = [dict(T=c, q_start=[s], kv_len=[s + c], qoff=s - starts[0])
+                          for s in starts]
+            qrows = (starts[0], self.L)
         self.dev = sd.make_inputs(self.B, H, G, D, DI, self.nb, self.L, self.seed, q_rows=qrows,
                                   b0=b0)
         T = self.calls[0]["T"]
@@ -219,12 +225,13 @@ class Job:
                 ev.append(e)
 
     def tokens(self):
-        return self.B * (1 if self.w["kind"] == "decode" else self.L)
+        return self.B * sum(c["T"] for c in self.calls)
 
     def positions(self):
         if self.w["kind"] == "decode":
             return np.full(self.B, self.L - 1, np.int64)
-        return np.arange(self.L, dtype=np.int64)
+        return np.concatenate([np.arange(c["q_start"][0], c["q_start"][0] + c["T"], dtype=np.int64)
+                               for c in self.calls])
 
 
 def time_job(job, steps, warmup, world):

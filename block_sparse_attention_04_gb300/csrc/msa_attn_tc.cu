@@ -477,9 +477,11 @@ cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  int per_sm = 1;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_tc_kernel<D>, kAttnThreads, C::kSmem);
-  const int grid = sm_count() * (per_sm > 0 ? per_sm : 1);
+  // Two CTAs per SM fit (2 x 256 TMEM columns, 2 x ~100 KiB smem, 84
+  // registers); ask for the shared-memory carveout that allows it.  CTAs do
+  // not depend on one another, so fewer resident CTAs only serialise.
+  cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  const int grid = 2 * sm_count();
   const int tp_max = pass_len(s);
   const int hpg = s.H / s.G;
   for (int t0 = 0; t0 < s.T; t0 += tp_max) {
