@@ -192,6 +192,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[31])
       : "r"(taddr));
 }
+// 32 lanes x 64 consecutive fp32 columns (two x32 loads, no wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+#define MSA_R(i) "=r"(r[i])
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : MSA_R(0), MSA_R(1), MSA_R(2), MSA_R(3), MSA_R(4), MSA_R(5), MSA_R(6), MSA_R(7),
+        MSA_R(8), MSA_R(9), MSA_R(10), MSA_R(11), MSA_R(12), MSA_R(13), MSA_R(14), MSA_R(15),
+        MSA_R(16), MSA_R(17), MSA_R(18), MSA_R(19), MSA_R(20), MSA_R(21), MSA_R(22), MSA_R(23),
+        MSA_R(24), MSA_R(25), MSA_R(26), MSA_R(27), MSA_R(28), MSA_R(29), MSA_R(30), MSA_R(31)
+      : "r"(taddr));
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : MSA_R(32), MSA_R(33), MSA_R(34), MSA_R(35), MSA_R(36), MSA_R(37), MSA_R(38), MSA_R(39),
+        MSA_R(40), MSA_R(41), MSA_R(42), MSA_R(43), MSA_R(44), MSA_R(45), MSA_R(46), MSA_R(47),
+        MSA_R(48), MSA_R(49), MSA_R(50), MSA_R(51), MSA_R(52), MSA_R(53), MSA_R(54), MSA_R(55),
+        MSA_R(56), MSA_R(57), MSA_R(58), MSA_R(59), MSA_R(60), MSA_R(61), MSA_R(62), MSA_R(63)
+      : "r"(taddr + 32));
+#undef MSA_R
+}
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

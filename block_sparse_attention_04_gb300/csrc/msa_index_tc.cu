@@ -4,15 +4,20 @@
 //
 // Rows are (query, group) pairs, r = (b*T + i)*G + g, so one Q_idx tile of
 // 128 rows is 128/G queries x G groups and every group reuses the same K_idx
-// tile.  One work item = 2 row tiles (256 rows) x one split of at most
-// kSplitBlocks key blocks.  Per item and key block (128 keys):
-//   warp 0      TMA: the two Q_idx tiles once per item, K_idx tiles through a
+// tile.  One work item = one row tile x one split of at most kSplitBlocks
+// key blocks; a one-CTA pre-pass lists the items that have key blocks,
+// heaviest first, and CTAs take them round-robin.  Per item and pair of key
+// blocks (256 keys, one MMA of N 256 per 16 dims: a tcgen05.mma costs a fixed
+// issue time, so each one is made large):
+//   warp 0      TMA: the Q_idx tile once per item, K_idx block pairs through a
 //               kStages-deep shared-memory ring;
-//   warp 1      tcgen05.mma (M 128, N 128, K Di, bf16 in, fp32 accumulate)
-//               for both row tiles into one of two TMEM accumulator stages;
-//   warps 2-9   epilogue: tcgen05.ld of the 128 fp32 scores of its row,
-//               block maximum (3-input max), insertion into the row's
-//               register-resident top-15 (score desc, block id asc).
+//   warp 1      tcgen05.mma (M 128, N 256, K Di, bf16 in, fp32 accumulate)
+//               into one of two TMEM accumulator stages;
+//   warps 2-9   epilogue: warpgroup 0 takes the even block of each pair,
+//               warpgroup 1 the odd one: tcgen05.ld of the row's 128 fp32
+//               scores, block maximum (3-input max tree), insertion into a
+//               register-resident top-15 (score desc, block id asc); the two
+//               lists merge through shared memory at the end of the item.
 // The [query x block] score matrix never leaves TMEM/registers.  Each item
 // writes its rows' partial top-15 lists; the streaming path's k-way merge
 // (topk_merge) adds the local block and sorts.
@@ -26,51 +31,122 @@ namespace msa {
 namespace {
 
 constexpr int kTileRows = 128;
-constexpr int kItemRows = 2 * kTileRows;
+constexpr int kItemRows = kTileRows;   // (query, group) rows per work item
 constexpr int kSplitBlocks = 256;
-constexpr int kStages = 6;
-constexpr int kThreads = 320;  // 10 warps
+constexpr int kPairKeys = 2 * kBlock;  // keys per MMA (N) and per accumulator stage
+constexpr int kStages = 5;             // K_idx stages (two key blocks each) in flight
+constexpr int kAccStages = 2;          // TMEM accumulator stages of kPairKeys columns
+constexpr int kThreads = 320;          // 10 warps
 constexpr int kEpiWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 
 template <int DI>
 struct IdxCfg {
   static constexpr int kRowBytes = DI * 2;
-  static constexpr int kTileBytes = kTileRows * kRowBytes;
+  static constexpr int kBoxBytes = kBlock * kRowBytes;     // one key block of K_idx
+  static constexpr int kTileBytes = kTileRows * kRowBytes;  // one Q_idx row tile
+  static constexpr int kStageBytes = 2 * kBoxBytes;         // two key blocks
   static constexpr uint32_t kSwz = DI == 64 ? kSwizzle128B : kSwizzle64B;
   static constexpr uint32_t kSbo = 8 * kRowBytes;  // one 8-row swizzle atom
   static constexpr int kKSteps = DI / 16;
-  static constexpr int kSmemA = 2 * 2 * kTileBytes;         // 2 buffers x 2 row tiles
-  static constexpr int kSmemB = kStages * kTileBytes;
-  static constexpr int kSmemBar = 256;
-  static constexpr int kSmem = kSmemA + kSmemB + kSmemBar + 1024;  // + alignment slack
+  static constexpr int kSmemA = 2 * kTileBytes;             // 2 buffers
+  static constexpr int kSmemB = kStages * kStageBytes;
+  static constexpr int kSmemX = kTileRows * kCand * 8;      // odd-block lists at item end
+  static constexpr int kSmemBar = 512;
+  static constexpr int kSmem = kSmemA + kSmemB + kSmemX + kSmemBar + 1024;  // + alignment
 };
 
 struct IndexTcArgs {
   Shape s;
   Positions pos;
-  int npairs;   // item row pairs per sequence
-  int nsplit;   // splits per pair (the merge's list count per row)
-  int nitems;
-  int64_t cap;  // K_idx rows per sequence
+  int npairs;         // row tiles per sequence
+  int nsplit;         // splits per row tile (the merge's list count per row)
+  int64_t cap;        // K_idx rows per sequence
+  const int32_t* items;  // packed (b, tile, split), heaviest first
+  const int32_t* nitems;
   Cand* cand;
   int* status;
 };
 
-// Work item -> sequence b, row pair p, split sp and key-block range [k0, k1).
-// Pairs are visited last-first (the longest key ranges first).
-__device__ __forceinline__ bool item_range(const IndexTcArgs& a, int item, int& b, int& p, int& sp,
-                                           int& k0, int& k1) {
-  const int per_b = a.npairs * a.nsplit;
-  b = item / per_b;
-  const int rem = item - b * per_b;
-  p = a.npairs - 1 - rem / a.nsplit;
-  sp = rem % a.nsplit;
-  const int i_last = min(a.s.T - 1, ((p + 1) * kItemRows - 1) / a.s.G);
-  const int kb_end = (int)(((int64_t)a.pos.q_start[b] + i_last) / kBlock);
+// packed work item: split (7 bits) | b (8 bits) | row tile (17 bits)
+__host__ __device__ __forceinline__ int32_t pack_item(int b, int p, int sp) {
+  return (int32_t)(((uint32_t)p << 15) | ((uint32_t)b << 7) | (uint32_t)sp);
+}
+
+__device__ __forceinline__ int pair_kb_end(const Shape& s, const Positions& pos, int b, int p) {
+  const int i_last = min(s.T - 1, ((p + 1) * kItemRows - 1) / s.G);
+  return (int)(((int64_t)pos.q_start[b] + i_last) / kBlock);
+}
+
+// Dense list of the work items that have key blocks, heaviest first: row
+// tiles in descending order (their key ranges grow), each tile's splits in order.
+__global__ void __launch_bounds__(1024) index_items_kernel(Shape s, Positions pos, int npairs,
+                                                           int32_t* items, int32_t* nitems) {
+  __shared__ int64_t part[1024];
+  const int64_t n = (int64_t)s.B * npairs;
+  const int64_t per = (n + 1023) / 1024;
+  const int64_t lo = threadIdx.x * per, hi = min(n, lo + per);
+  // global tile order q: q = (npairs-1-p) * B + b
+  int64_t cnt = 0;
+  for (int64_t q = lo; q < hi; ++q) {
+    const int b = (int)(q % s.B), p = npairs - 1 - (int)(q / s.B);
+    cnt += (pair_kb_end(s, pos, b, p) + kSplitBlocks - 1) / kSplitBlocks;
+  }
+  part[threadIdx.x] = cnt;
+  __syncthreads();
+  for (int d = 1; d < 1024; d <<= 1) {
+    int64_t v = (int)threadIdx.x >= d ? part[threadIdx.x - d] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int64_t o = part[threadIdx.x] - cnt;
+  for (int64_t q = lo; q < hi; ++q) {
+    const int b = (int)(q % s.B), p = npairs - 1 - (int)(q / s.B);
+    const int c = (pair_kb_end(s, pos, b, p) + kSplitBlocks - 1) / kSplitBlocks;
+    for (int sp = 0; sp < c; ++sp) items[o++] = pack_item(b, p, sp);
+  }
+  if (threadIdx.x == 1023) *nitems = (int32_t)part[1023];
+}
+
+__device__ __forceinline__ void item_range(const IndexTcArgs& a, int32_t packed, int& b, int& p,
+                                           int& sp, int& k0, int& k1) {
+  sp = packed & 127;
+  b = (packed >> 7) & 255;
+  p = (int)((uint32_t)packed >> 15);
   k0 = sp * kSplitBlocks;
-  k1 = min(k0 + kSplitBlocks, kb_end);
-  return k0 < k1;
+  k1 = min(k0 + kSplitBlocks, pair_kb_end(a.s, a.pos, b, p));
+}
+
+// max of 128 fp32 values held as bits, as a tree of 3-input maxima
+__device__ __forceinline__ float max128(const uint32_t (&v)[128]) {
+  float l1[43];
+#pragma unroll
+  for (int k = 0; k < 42; ++k)
+    l1[k] = fmax3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]), __uint_as_float(v[3 * k + 2]));
+  l1[42] = fmaxf(__uint_as_float(v[126]), __uint_as_float(v[127]));
+  float l2[15];
+#pragma unroll
+  for (int k = 0; k < 14; ++k) l2[k] = fmax3(l1[3 * k], l1[3 * k + 1], l1[3 * k + 2]);
+  l2[14] = l1[42];
+  float l3[5];
+#pragma unroll
+  for (int k = 0; k < 5; ++k) l3[k] = fmax3(l2[3 * k], l2[3 * k + 1], l2[3 * k + 2]);
+  return fmax3(fmax3(l3[0], l3[1], l3[2]), l3[3], l3[4]);
+}
+
+// Insert (score, id) into a list sorted by (score desc, id asc).
+__device__ __forceinline__ void list_insert(float (&sc)[kCand], int (&id)[kCand], float cs, int ci) {
+#pragma unroll
+  for (int j = 0; j < kCand; ++j) {
+    const bool better = cs > sc[j] || (cs == sc[j] && ci < id[j]);
+    const float tsc = sc[j];
+    const int tid = id[j];
+    sc[j] = better ? cs : tsc;
+    id[j] = better ? ci : tid;
+    cs = better ? tsc : cs;
+    ci = better ? tid : ci;
+  }
 }
 
 template <int DI>
@@ -80,21 +156,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = IdxCfg<DI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t* sA = smem;                 // [abuf][tile][128 rows][DI]
-  uint8_t* sB = smem + C::kSmemA;     // [stage][128 keys][DI]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kSmemA + C::kSmemB);
-  uint64_t* full = bars;                      // kStages
-  uint64_t* empty = bars + kStages;           // kStages
-  uint64_t* a_full = bars + 2 * kStages;      // 2
-  uint64_t* a_empty = a_full + 2;             // 2
-  uint64_t* tm_full = a_empty + 2;            // 2
-  uint64_t* tm_empty = tm_full + 2;           // 2
-  uint64_t* mma_done = tm_empty + 2;          // 1
+  uint8_t* sA = smem;                              // [abuf][128 rows][DI]
+  uint8_t* sB = smem + C::kSmemA;                  // [stage][256 keys][DI]
+  Cand* sX = reinterpret_cast<Cand*>(sB + C::kSmemB);  // [15][128 rows]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sX) + C::kSmemX);
+  uint64_t* full = bars;                          // kStages
+  uint64_t* empty = full + kStages;               // kStages
+  uint64_t* a_full = empty + kStages;             // 2
+  uint64_t* a_empty = a_full + 2;                 // 2
+  uint64_t* tm_full = a_empty + 2;                // kAccStages
+  uint64_t* tm_empty = tm_full + kAccStages;      // kAccStages
+  uint64_t* mma_done = tm_empty + kAccStages;     // 1
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* epi_stop = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
+    *epi_stop = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
@@ -102,6 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&a_full[i], 1);
       mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < kAccStages; ++i) {
       mbar_init(&tm_full[i], 1);
       mbar_init(&tm_empty[i], kEpiWarps);
     }
@@ -117,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int T = a.s.T, G = a.s.G;
+  const int nitems = *a.nitems;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
@@ -124,21 +206,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, abuf = 0;
       uint32_t sphase = 0, aphase = 0;
       int issued = 0;
-      for (int item = blockIdx.x; item < a.nitems && !*abort_flag; item += gridDim.x) {
+      for (int it = blockIdx.x; it < nitems && !*abort_flag; it += gridDim.x) {
         int b, p, sp, k0, k1;
-        if (!item_range(a, item, b, p, sp, k0, k1)) continue;
+        item_range(a, a.items[it], b, p, sp, k0, k1);
         if (!mbar_wait(&a_empty[abuf], aphase ^ 1, a.status)) { *abort_flag = 1; break; }
-        mbar_arrive_expect_tx(&a_full[abuf], 2 * C::kTileBytes);
-        const int row0 = (b * T) * G + p * kItemRows;
-        tma_load_2d(smem_u32(sA + (abuf * 2 + 0) * C::kTileBytes), &tm_q, &a_full[abuf], 0, row0);
-        tma_load_2d(smem_u32(sA + (abuf * 2 + 1) * C::kTileBytes), &tm_q, &a_full[abuf], 0,
-                    row0 + kTileRows);
+        mbar_arrive_expect_tx(&a_full[abuf], C::kTileBytes);
+        tma_load_2d(smem_u32(sA + abuf * C::kTileBytes), &tm_q, &a_full[abuf], 0,
+                    (b * T) * G + p * kItemRows);
         if (++abuf == 2) { abuf = 0; aphase ^= 1; }
-        for (int kb = k0; kb < k1; ++kb) {
+        for (int kb = k0; kb < k1; kb += 2) {
           if (!mbar_wait(&empty[stage], sphase ^ 1, a.status)) { *abort_flag = 1; break; }
-          mbar_arrive_expect_tx(&full[stage], C::kTileBytes);
-          tma_load_2d(smem_u32(sB + stage * C::kTileBytes), &tm_k, &full[stage], 0,
-                      (int)(b * a.cap + (int64_t)kb * kBlock));
+          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+          const uint32_t dst = smem_u32(sB + stage * C::kStageBytes);
+          const int row = (int)(b * a.cap + (int64_t)kb * kBlock);
+          // the second block may lie past the item's range (odd count): its
+          // scores are ignored; past the tensor's end the copy reads zeros
+          tma_load_2d(dst, &tm_k, &full[stage], 0, row);
+          tma_load_2d(dst + C::kBoxBytes, &tm_k, &full[stage], 0, row + kBlock);
           ++issued;
           if (++stage == kStages) { stage = 0; sphase ^= 1; }
         }
@@ -157,37 +241,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc = idesc_bf16(128, kPairKeys, false, false);
       int stage = 0, abuf = 0, ts = 0;
       uint32_t sphase = 0, aphase = 0, tphase = 0;
-      for (int item = blockIdx.x; item < a.nitems && !*abort_flag; item += gridDim.x) {
+      for (int it = blockIdx.x; it < nitems && !*abort_flag; it += gridDim.x) {
         int b, p, sp, k0, k1;
-        if (!item_range(a, item, b, p, sp, k0, k1)) continue;
+        item_range(a, a.items[it], b, p, sp, k0, k1);
         if (!mbar_wait(&a_full[abuf], aphase, a.status)) { *abort_flag = 1; break; }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(sA + (abuf * 2 + 0) * C::kTileBytes);
-        const uint32_t a1 = smem_u32(sA + (abuf * 2 + 1) * C::kTileBytes);
-        for (int kb = k0; kb < k1; ++kb) {
+        const uint32_t a0 = smem_u32(sA + abuf * C::kTileBytes);
+        bool ok = true;
+        for (int kb = k0; kb < k1; kb += 2) {
           if (!mbar_wait(&full[stage], sphase, a.status) ||
               !mbar_wait(&tm_empty[ts], tphase ^ 1, a.status)) {
-            *abort_flag = 1;
+            ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t bsm = smem_u32(sB + stage * C::kTileBytes);
-          const uint32_t d0 = tmem + ts * 256;
+          const uint32_t bsm = smem_u32(sB + stage * C::kStageBytes);
 #pragma unroll
-          for (int k = 0; k < C::kKSteps; ++k) {
-            const uint64_t bd = smem_desc(bsm + k * 32, 16, C::kSbo, C::kSwz);
-            tc_mma_f16(d0, smem_desc(a0 + k * 32, 16, C::kSbo, C::kSwz), bd, idesc, k > 0);
-            tc_mma_f16(d0 + 128, smem_desc(a1 + k * 32, 16, C::kSbo, C::kSwz), bd, idesc, k > 0);
-          }
-          tc_commit(&empty[stage]);
+          for (int k = 0; k < C::kKSteps; ++k)
+            tc_mma_f16(tmem + ts * kPairKeys, smem_desc(a0 + k * 32, 16, C::kSbo, C::kSwz),
+                       smem_desc(bsm + k * 32, 16, C::kSbo, C::kSwz), idesc, k > 0);
           tc_commit(&tm_full[ts]);
+          tc_commit(&empty[stage]);
+          if (++ts == kAccStages) { ts = 0; tphase ^= 1; }
           if (++stage == kStages) { stage = 0; sphase ^= 1; }
-          if (++ts == 2) { ts = 0; tphase ^= 1; }
         }
-        if (*abort_flag) break;
+        if (!ok) { *abort_flag = 1; break; }
         tc_commit(&a_empty[abuf]);
         if (++abuf == 2) { abuf = 0; aphase ^= 1; }
       }
@@ -197,16 +278,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ----------------------------------------------------------- epilogue
-    const int ew = warp - 2;
-    const int tile = ew >> 2;
-    const int quad = warp & 3;  // TMEM lanes this warp may access: 32*quad ..
-    const int row_in_item = tile * kTileRows + quad * 32 + lane;
+    // warpgroup wg (warps 2-5: 0, warps 6-9: 1) owns the key block 2j + wg of
+    // every stage; TMEM lanes 32*quad .. of its row tile
+    const int wg = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + wg * kBlock;
     int ts = 0;
     uint32_t tphase = 0;
-    for (int item = blockIdx.x; item < a.nitems && !*abort_flag; item += gridDim.x) {
+    // The 8 epilogue warps meet at two named barriers per item, which have no
+    // timeout; they stop together, on a shared stop word written before the
+    // second barrier and read after it.
+    bool stop = false;
+    for (int it = blockIdx.x; it < nitems && !stop; it += gridDim.x) {
       int b, p, sp, k0, k1;
-      if (!item_range(a, item, b, p, sp, k0, k1)) continue;
-      const int local = p * kItemRows + row_in_item;  // row within sequence b
+      item_range(a, a.items[it], b, p, sp, k0, k1);
+      const int local = p * kItemRows + r;  // row within sequence b
       const bool valid = local < T * G;
       const int qi = local / G, g = local - (local / G) * G;
       const int lb = valid ? (int)(((int64_t)a.pos.q_start[b] + qi) / kBlock) : 0;
@@ -218,56 +305,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         id[j] = INT_MAX;
       }
       bool ok = true;
-      for (int kb = k0; kb < k1; ++kb) {
-        // warp-uniform: a timeout in any lane stops the whole warp before the
-        // .sync.aligned TMEM loads
-        if (!__all_sync(0xffffffffu, mbar_wait(&tm_full[ts], tphase, a.status))) {
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
+      for (int kb = k0; kb < k1; kb += 2) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&tm_full[ts], tphase, a.status))) { ok = false; break; }
         tc_fence_after();
-        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + ts * 256 + tile * 128;
-        uint32_t v[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(taddr + c * 32, v[c]);
+        uint32_t v[128];
+        tmem_ld64(lane_base + ts * kPairKeys, *reinterpret_cast<uint32_t(*)[64]>(&v[0]));
+        tmem_ld64(lane_base + ts * kPairKeys + 64, *reinterpret_cast<uint32_t(*)[64]>(&v[64]));
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tm_empty[ts]);
-        if (++ts == 2) { ts = 0; tphase ^= 1; }
-        float m[4];
+        if (++ts == kAccStages) { ts = 0; tphase ^= 1; }
+        const float mb = max128(v);
+        const int blk = kb + wg;
+        if (valid && blk < k1 && blk < lb && mb > sc[kCand - 1]) list_insert(sc, id, mb, blk);
+      }
+      // merge the odd-block list (warpgroup 1) into the even-block list
+      if (wg == 1) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float x = fmax3(__uint_as_float(v[c][0]), __uint_as_float(v[c][1]), __uint_as_float(v[c][2]));
+        for (int j = 0; j < kCand; ++j) sX[j * kTileRows + r] = Cand{sc[j], id[j]};
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (wg == 0 && ok) {
 #pragma unroll
-          for (int e = 3; e < 31; e += 2)
-            x = fmax3(x, __uint_as_float(v[c][e]), __uint_as_float(v[c][e + 1]));
-          m[c] = fmaxf(x, __uint_as_float(v[c][31]));
+        for (int j = 0; j < kCand; ++j) {
+          const Cand c = sX[j * kTileRows + r];
+          if (c.score > sc[kCand - 1] || (c.score == sc[kCand - 1] && c.id < id[kCand - 1]))
+            list_insert(sc, id, c.score, c.id);
         }
-        const float mb = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
-        if (valid && kb < lb && mb > sc[kCand - 1]) {
-          float cs = mb;
-          int ci = kb;
+        if (valid) {
+          Cand* out = a.cand + ((((size_t)b * T + qi) * a.nsplit + sp) * G + g) * kCand;
 #pragma unroll
-          for (int j = 0; j < kCand; ++j) {
-            const bool better = cs > sc[j] || (cs == sc[j] && ci < id[j]);
-            const float tsc = sc[j];
-            const int tid = id[j];
-            sc[j] = better ? cs : tsc;
-            id[j] = better ? ci : tid;
-            cs = better ? tsc : cs;
-            ci = better ? tid : ci;
-          }
+          for (int j = 0; j < kCand; ++j) out[j] = Cand{sc[j], id[j]};
         }
       }
-      if (!ok) break;
-      if (valid) {
-        Cand* out = a.cand + ((((size_t)b * T + qi) * a.nsplit + sp) * G + g) * kCand;
-#pragma unroll
-        for (int j = 0; j < kCand; ++j) out[j] = Cand{sc[j], id[j]};
-      }
+      if (!ok || *abort_flag) *epi_stop = 1;
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      stop = *epi_stop != 0;
     }
+    if (stop) *abort_flag = 1;
   }
 
   tc_fence_before();
@@ -281,6 +357,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 int index_tc_nsplit(int max_blocks) {
   const int n = (max_blocks - 1 + kSplitBlocks - 1) / kSplitBlocks;
   return n > 0 ? n : 1;
+}
+
+int index_tc_npairs(const Shape& s) {
+  return (int)((s.T * (int64_t)s.G + kItemRows - 1) / kItemRows);
+}
+
+// scratch layout: [candidate lists][item count (256 B)][items]
+size_t cand_bytes(const Shape& s) {
+  const size_t c = (size_t)s.B * s.T * index_tc_nsplit(s.max_blocks) * s.G * kCand * sizeof(Cand);
+  return (c + 255) / 256 * 256;
+}
+
+size_t items_cap(const Shape& s) {
+  return (size_t)s.B * index_tc_npairs(s) * index_tc_nsplit(s.max_blocks);
 }
 
 template <int DI>
@@ -307,20 +397,26 @@ cudaError_t launch_index_tc_impl(const Shape& s, const Positions& pos, const uin
                          DI == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
   }
+  char* base = reinterpret_cast<char*>(ws.cand);
+  int32_t* nitems = reinterpret_cast<int32_t*>(base + cand_bytes(s));
+  int32_t* items = nitems + 64;
   IndexTcArgs a;
   a.s = s;
   a.pos = pos;
-  a.npairs = (int)((s.T * (int64_t)s.G + kItemRows - 1) / kItemRows);
+  a.npairs = index_tc_npairs(s);
   a.nsplit = index_tc_nsplit(s.max_blocks);
-  a.nitems = s.B * a.npairs * a.nsplit;
   a.cap = cap;
+  a.items = items;
+  a.nitems = nitems;
   a.cand = ws.cand;
   a.status = ws.status;
   cudaError_t e = cudaFuncSetAttribute(index_tc_kernel<DI>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  const int grid = a.nitems < sm_count() ? a.nitems : sm_count();
-  note_launches(1);
+  const size_t maxitems = items_cap(s);
+  const int grid = maxitems < (size_t)sm_count() ? (int)maxitems : sm_count();
+  note_launches(2);
+  index_items_kernel<<<1, 1024, 0, st>>>(s, pos, a.npairs, items, nitems);
   index_tc_kernel<DI><<<grid, kThreads, C::kSmem, st>>>(tm_q, tm_k, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -330,7 +426,7 @@ cudaError_t launch_index_tc_impl(const Shape& s, const Positions& pos, const uin
 }  // namespace
 
 size_t tc_index_workspace_bytes(const Shape& s) {
-  return (size_t)s.B * s.T * index_tc_nsplit(s.max_blocks) * s.G * kCand * sizeof(Cand);
+  return cand_bytes(s) + 256 + items_cap(s) * sizeof(int32_t);
 }
 
 cudaError_t launch_index_tc(const Shape& s, const Positions& pos, const uint16_t* q_idx,
