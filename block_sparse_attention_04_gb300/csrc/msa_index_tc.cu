@@ -135,6 +135,27 @@ __device__ __forceinline__ float max128(const uint32_t (&v)[128]) {
   return fmax3(fmax3(l3[0], l3[1], l3[2]), l3[3], l3[4]);
 }
 
+// Insert (cs, ci) into a list sorted by (score desc, id asc) when ci is larger
+// than every id in the list (blocks are scanned in increasing order): its slot
+// is the number of entries with score >= cs, and everything from there shifts
+// down by one.  The caller checks cs > sc[last] first.  All steps are
+// independent, so the update is short and has no serial chain.
+__device__ __forceinline__ void list_insert_newest(float (&sc)[kCand], int (&id)[kCand], float cs,
+                                                   int ci) {
+  int k = 0;
+#pragma unroll
+  for (int j = 0; j < kCand; ++j) k += sc[j] >= cs ? 1 : 0;
+#pragma unroll
+  for (int j = kCand - 1; j > 0; --j) {
+    sc[j] = j > k ? sc[j - 1] : (j == k ? cs : sc[j]);
+    id[j] = j > k ? id[j - 1] : (j == k ? ci : id[j]);
+  }
+  if (k == 0) {
+    sc[0] = cs;
+    id[0] = ci;
+  }
+}
+
 // Insert (score, id) into a list sorted by (score desc, id asc).
 __device__ __forceinline__ void list_insert(float (&sc)[kCand], int (&id)[kCand], float cs, int ci) {
 #pragma unroll
@@ -318,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++ts == kAccStages) { ts = 0; tphase ^= 1; }
         const float mb = max128(v);
         const int blk = kb + wg;
-        if (valid && blk < k1 && blk < lb && mb > sc[kCand - 1]) list_insert(sc, id, mb, blk);
+        if (valid && blk < k1 && blk < lb && mb > sc[kCand - 1]) list_insert_newest(sc, id, mb, blk);
       }
       // merge the odd-block list (warpgroup 1) into the even-block list
       if (wg == 1) {
