@@ -13,10 +13,11 @@
 //               kStages-deep shared-memory ring;
 //   warp 1      tcgen05.mma (M 128, N 256, K Di, bf16 in, fp32 accumulate)
 //               into one of two TMEM accumulator stages;
-//   warps 2-9   epilogue: warpgroup 0 takes the even block of each pair,
-//               warpgroup 1 the odd one: tcgen05.ld of the row's 128 fp32
-//               scores, block maximum (3-input max tree), insertion into a
-//               register-resident top-15 (score desc, block id asc); the two
+//   warps 2-17  epilogue, four warpgroups: two read each accumulator stage
+//               (one key block each), stages alternate between the two
+//               pairs; tcgen05.ld of the row's 128 fp32 scores in 32-column
+//               chunks, block maximum (3-input max), insertion into a
+//               register-resident top-15 (score desc, block id asc); the four
 //               lists merge through shared memory at the end of the item.
 // The [query x block] score matrix never leaves TMEM/registers.  Each item
 // writes its rows' partial top-15 lists; the streaming path's k-way merge
@@ -34,10 +35,10 @@ constexpr int kTileRows = 128;
 constexpr int kItemRows = kTileRows;   // (query, group) rows per work item
 constexpr int kSplitBlocks = 256;
 constexpr int kPairKeys = 2 * kBlock;  // keys per MMA (N) and per accumulator stage
-constexpr int kStages = 5;             // K_idx stages (two key blocks each) in flight
+constexpr int kStages = 4;             // K_idx stages (two key blocks each) in flight
 constexpr int kAccStages = 2;          // TMEM accumulator stages of kPairKeys columns
-constexpr int kThreads = 320;          // 10 warps
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;          // 4 warpgroups
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
 constexpr uint32_t kTmemCols = 512;
 
 template <int DI>
@@ -51,7 +52,7 @@ struct IdxCfg {
   static constexpr int kKSteps = DI / 16;
   static constexpr int kSmemA = 2 * kTileBytes;             // 2 buffers
   static constexpr int kSmemB = kStages * kStageBytes;
-  static constexpr int kSmemX = kTileRows * kCand * 8;      // odd-block lists at item end
+  static constexpr int kSmemX = 2 * kTileRows * kCand * 8;  // lists exchanged at item end
   static constexpr int kSmemBar = 512;
   static constexpr int kSmem = kSmemA + kSmemB + kSmemX + kSmemBar + 1024;  // + alignment
 };
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;                              // [abuf][128 rows][DI]
   uint8_t* sB = smem + C::kSmemA;                  // [stage][256 keys][DI]
-  Cand* sX = reinterpret_cast<Cand*>(sB + C::kSmemB);  // [15][128 rows]
+  Cand* sX = reinterpret_cast<Cand*>(sB + C::kSmemB);  // [2][15][128 rows]
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sX) + C::kSmemX);
   uint64_t* full = bars;                          // kStages
   uint64_t* empty = full + kStages;               // kStages
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kAccStages; ++i) {
       mbar_init(&tm_full[i], 1);
-      mbar_init(&tm_empty[i], kEpiWarps);
+      mbar_init(&tm_empty[i], kEpiWarps / 2);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -299,17 +300,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ----------------------------------------------------------- epilogue
-    // warpgroup wg (warps 2-5: 0, warps 6-9: 1) owns the key block 2j + wg of
-    // every stage; TMEM lanes 32*quad .. of its row tile
-    const int wg = (warp - 2) >> 2;
+    // Four warpgroups (warps 2-17).  Warpgroups 0 and 1 read accumulator
+    // stage 0, warpgroups 2 and 3 stage 1; within a stage, the even warpgroup
+    // of the pair takes the first key block, the odd one the second.  Stages
+    // alternate, so each warp has two stage-times per 128-score block.
+    const int wg = (warp - 2) >> 2;     // 0..3
+    const int my_ts = wg >> 1;          // accumulator stage this warpgroup reads
+    const int half = wg & 1;            // which key block of the stage
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + wg * kBlock;
-    int ts = 0;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + my_ts * kPairKeys +
+                               half * kBlock;
     uint32_t tphase = 0;
-    // The 8 epilogue warps meet at two named barriers per item, which have no
+    int gstage = 0;                     // global stage count of this CTA at the item start
+    // The 16 epilogue warps meet at named barriers per item, which have no
     // timeout; they stop together, on a shared stop word written before the
-    // second barrier and read after it.
+    // last barrier and read after it.
     bool stop = false;
     for (int it = blockIdx.x; it < nitems && !stop; it += gridDim.x) {
       int b, p, sp, k0, k1;
@@ -325,32 +331,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         sc[j] = -INFINITY;
         id[j] = INT_MAX;
       }
+      const int nst = (k1 - k0 + 1) >> 1;
       bool ok = true;
-      for (int kb = k0; kb < k1; kb += 2) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&tm_full[ts], tphase, a.status))) { ok = false; break; }
+      // this warpgroup's stages of the item: global index == my_ts (mod 2)
+      for (int q = ((my_ts - gstage) & 1); q < nst; q += 2) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&tm_full[my_ts], tphase, a.status))) { ok = false; break; }
+        tphase ^= 1;
         tc_fence_after();
-        uint32_t v[128];
-        tmem_ld64(lane_base + ts * kPairKeys, *reinterpret_cast<uint32_t(*)[64]>(&v[0]));
-        tmem_ld64(lane_base + ts * kPairKeys + 64, *reinterpret_cast<uint32_t(*)[64]>(&v[64]));
+        uint32_t v[32];
+        float m;
+        tmem_ld32(lane_base, v);
         tmem_ld_wait();
+        m = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+        for (int c = 1; c < 4; ++c) {
+          float mc[11];
+#pragma unroll
+          for (int k = 0; k < 10; ++k)
+            mc[k] = fmax3(__uint_as_float(v[3 * k + 2]), __uint_as_float(v[3 * k + 3]),
+                          __uint_as_float(v[3 * k + 4]));
+          mc[10] = __uint_as_float(v[31]);
+          tmem_ld32(lane_base + c * 32, v);
+          const float x = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]),
+                                fmax3(mc[6], mc[7], mc[8]));
+          m = fmax3(m, x, fmaxf(mc[9], mc[10]));
+          tmem_ld_wait();
+          m = fmax3(m, __uint_as_float(v[0]), __uint_as_float(v[1]));
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tm_empty[ts]);
-        if (++ts == kAccStages) { ts = 0; tphase ^= 1; }
-        const float mb = max128(v);
-        const int blk = kb + wg;
-        if (valid && blk < k1 && blk < lb && mb > sc[kCand - 1]) list_insert_newest(sc, id, mb, blk);
+        if (lane == 0) mbar_arrive(&tm_empty[my_ts]);
+        {
+          float mc[11];
+#pragma unroll
+          for (int k = 0; k < 10; ++k)
+            mc[k] = fmax3(__uint_as_float(v[3 * k + 2]), __uint_as_float(v[3 * k + 3]),
+                          __uint_as_float(v[3 * k + 4]));
+          mc[10] = __uint_as_float(v[31]);
+          const float x = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]),
+                                fmax3(mc[6], mc[7], mc[8]));
+          m = fmax3(m, x, fmaxf(mc[9], mc[10]));
+        }
+        const int blk = k0 + 2 * q + half;
+        if (valid && blk < k1 && blk < lb && m > sc[kCand - 1]) list_insert_newest(sc, id, m, blk);
       }
-      // merge the odd-block list (warpgroup 1) into the even-block list
+      gstage += nst;
+      // merge the four lists: 2 -> 0 and 3 -> 1, then 1 -> 0
+      Cand* x0 = sX;
+      Cand* x1 = sX + kCand * kTileRows;
+      if (wg >= 2) {
+        Cand* x = wg == 2 ? x0 : x1;
+#pragma unroll
+        for (int j = 0; j < kCand; ++j) x[j * kTileRows + r] = Cand{sc[j], id[j]};
+      }
+      asm volatile("bar.sync 1, 512;" ::: "memory");
+      if (wg < 2) {
+        const Cand* x = wg == 0 ? x0 : x1;
+#pragma unroll
+        for (int j = 0; j < kCand; ++j) {
+          const Cand c = x[j * kTileRows + r];
+          if (c.score > sc[kCand - 1] || (c.score == sc[kCand - 1] && c.id < id[kCand - 1]))
+            list_insert(sc, id, c.score, c.id);
+        }
+      }
+      asm volatile("bar.sync 1, 512;" ::: "memory");
       if (wg == 1) {
 #pragma unroll
-        for (int j = 0; j < kCand; ++j) sX[j * kTileRows + r] = Cand{sc[j], id[j]};
+        for (int j = 0; j < kCand; ++j) x0[j * kTileRows + r] = Cand{sc[j], id[j]};
       }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      asm volatile("bar.sync 1, 512;" ::: "memory");
       if (wg == 0 && ok) {
 #pragma unroll
         for (int j = 0; j < kCand; ++j) {
-          const Cand c = sX[j * kTileRows + r];
+          const Cand c = x0[j * kTileRows + r];
           if (c.score > sc[kCand - 1] || (c.score == sc[kCand - 1] && c.id < id[kCand - 1]))
             list_insert(sc, id, c.score, c.id);
         }
@@ -361,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok || *abort_flag) *epi_stop = 1;
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      asm volatile("bar.sync 1, 512;" ::: "memory");
       stop = *epi_stop != 0;
     }
     if (stop) *abort_flag = 1;
