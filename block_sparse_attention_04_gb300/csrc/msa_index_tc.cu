@@ -33,7 +33,7 @@ namespace {
 
 constexpr int kTileRows = 128;
 constexpr int kItemRows = kTileRows;   // (query, group) rows per work item
-constexpr int kSplitBlocks = 256;
+constexpr int kSplitBlocks = 512;
 constexpr int kPairKeys = 2 * kBlock;  // keys per MMA (N) and per accumulator stage
 constexpr int kStages = 4;             // K_idx stages (two key blocks each) in flight
 constexpr int kAccStages = 2;          // TMEM accumulator stages of kPairKeys columns
