@@ -164,19 +164,21 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   uint8_t* sK = smem + C::kSmemQ;
   uint8_t* sV = sK + C::kSmemK;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + C::kSmemV);
-  uint64_t* bar_kv = bars + 0;
+  uint64_t* bar_k = bars + 0;
   uint64_t* bar_q = bars + 1;
   uint64_t* bar_s = bars + 2;
   uint64_t* bar_p = bars + 3;
   uint64_t* bar_o = bars + 4;
   uint64_t* bar_done = bars + 5;
   uint64_t* bar_fin = bars + 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
+  uint64_t* bar_v = bars + 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(bar_kv, 1);
+    mbar_init(bar_k, 1);
+    mbar_init(bar_v, 1);
     mbar_init(bar_q, 128);
     mbar_init(bar_s, 1);
     mbar_init(bar_p, 128);
@@ -202,7 +204,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   const int tile_lo = blockIdx.x * per;
   const int tile_hi = min(ntiles, tile_lo + per);
   uint32_t it = 0;      // tiles processed by this CTA (phase of the per-tile barriers)
-  uint32_t kv_it = 0;   // K/V loads issued by this CTA (phase of bar_kv)
+  uint32_t kv_it = 0;   // K/V loads issued by this CTA (phase of bar_k, bar_v)
   int prev_list = -1;
   for (int tile = tile_lo; tile < tile_hi; ++tile, ++it) {
     if (*abort_flag) break;
@@ -222,17 +224,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 
     if (warp < 4) {
       // -------------------------------------------------- loads (warps 0-3)
+      // Q and K of this tile once S of the previous tile is done (P lives in
+      // TMEM, so the Q buffer is free then); V once its P.V is done.
       if (it > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_o, ph ^ 1, a.status))) { *abort_flag = 1; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_s, ph ^ 1, a.status))) { *abort_flag = 1; break; }
       }
+      const int row = (int)(((int64_t)b * a.s.max_blocks + kb) * kBlock);
       if (warp == 0 && lane == 0 && !reuse_kv) {
-        mbar_arrive_expect_tx(bar_kv, 2 * C::kNHalf * C::kHalf);
-        const int row = (int)(((int64_t)b * a.s.max_blocks + kb) * kBlock);
+        mbar_arrive_expect_tx(bar_k, C::kNHalf * C::kHalf);
 #pragma unroll
-        for (int h = 0; h < C::kNHalf; ++h) {
-          tma_load_3d(smem_u32(sK + h * C::kHalf), &tm_k, bar_kv, h * 64, g, row);
-          tma_load_3d(smem_u32(sV + h * C::kHalf), &tm_v, bar_kv, h * 64, g, row);
-        }
+        for (int h = 0; h < C::kNHalf; ++h)
+          tma_load_3d(smem_u32(sK + h * C::kHalf), &tm_k, bar_k, h * 64, g, row);
       }
       // Q rows: row r = entry e * hpg + head hh; 16-byte chunks, swizzled
       constexpr int kChunks = D / 8;
@@ -248,13 +250,22 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       cp_async_wait<0>();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(bar_q);
+      if (it > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_o, ph ^ 1, a.status))) { *abort_flag = 1; break; }
+      }
+      if (warp == 0 && lane == 0 && !reuse_kv) {
+        mbar_arrive_expect_tx(bar_v, C::kNHalf * C::kHalf);
+#pragma unroll
+        for (int h = 0; h < C::kNHalf; ++h)
+          tma_load_3d(smem_u32(sV + h * C::kHalf), &tm_v, bar_v, h * 64, g, row);
+      }
     } else if (warp == 8) {
       // -------------------------------------------------- MMA (warp 8)
       bool ok = true;
       if (lane == 0) {
         constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
         constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
-        ok = mbar_wait(bar_q, ph, a.status) && mbar_wait(bar_kv, kv_ph, a.status) &&
+        ok = mbar_wait(bar_q, ph, a.status) && mbar_wait(bar_k, kv_ph, a.status) &&
              (it == 0 || mbar_wait(bar_done, ph ^ 1, a.status));
         if (ok) {
           tc_fence_after();
@@ -266,15 +277,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                        smem_desc(k0 + off, 16, 1024, kSwizzle128B), idesc_s, k > 0);
           }
           tc_commit(bar_s);
-          ok = mbar_wait(bar_p, ph, a.status);
+          ok = mbar_wait(bar_p, ph, a.status) && mbar_wait(bar_v, kv_ph, a.status);
           if (ok) {
             tc_fence_after();
+            // P (bf16, two per column) is in TMEM columns [0, 64): 8 per 16 tokens
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {  // 16 tokens per step
-              const uint32_t aoff = (k >> 2) * C::kHalf + (k & 3) * 32;
-              tc_mma_f16(tmem + 128, smem_desc(q0 + aoff, 16, 1024, kSwizzle128B),
-                         smem_desc(v0 + k * 2048, C::kHalf, 1024, kSwizzle128B), idesc_o, k > 0);
-            }
+            for (int k = 0; k < 8; ++k)
+              tc_mma_f16_ts(tmem + 128, tmem + k * 8,
+                            smem_desc(v0 + k * 2048, C::kHalf, 1024, kSwizzle128B), idesc_o, k > 0);
             tc_commit(bar_o);
           }
         }
@@ -310,31 +320,26 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         for (int e = 0; e < 32; ++e)
           if (c * 32 + e <= lim) m = fmaxf(m, __uint_as_float(v[e]) * sl);
       }
-      // pass 2: P = 2^(s - m) as bf16 into the swizzled P tile (over Q), row sum
+      // pass 2: P = 2^(s - m) as bf16, two per column, written over S in TMEM
+      // (chunk c of S is read before columns [16c, 16c+16) are written, and
+      // those columns belong to chunks already read); row sum
       float l = 0.f;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(lane_base + c * 32, v);
         tmem_ld_wait();
+        uint32_t w[16];
 #pragma unroll
-        for (int e8 = 0; e8 < 4; ++e8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int e = e8 * 8 + 2 * u;
-            const float p0 = (c * 32 + e <= lim) ? ex2(__uint_as_float(v[e]) * sl - m) : 0.f;
-            const float p1 = (c * 32 + e + 1 <= lim) ? ex2(__uint_as_float(v[e + 1]) * sl - m) : 0.f;
-            l += p0 + p1;
-            w[u] = pack_bf16(p0, p1);
-          }
-          const int chunk = c * 4 + e8;  // 8 tokens per chunk, 16 per row
-          const uint32_t addr = smem_u32(sQ + (chunk >> 3) * C::kHalf + sw128(r, chunk & 7));
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
-                       "r"(w[2]), "r"(w[3])
-                       : "memory");
+        for (int u = 0; u < 16; ++u) {
+          const int e = 2 * u;
+          const float p0 = (c * 32 + e <= lim) ? ex2(__uint_as_float(v[e]) * sl - m) : 0.f;
+          const float p1 = (c * 32 + e + 1 <= lim) ? ex2(__uint_as_float(v[e + 1]) * sl - m) : 0.f;
+          l += p0 + p1;
+          w[u] = pack_bf16(p0, p1);
         }
+        tmem_st16(lane_base + c * 16, w);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_p);
       if (!__all_sync(0xffffffffu, mbar_wait(bar_o, ph, a.status))) { *abort_flag = 1; break; }
