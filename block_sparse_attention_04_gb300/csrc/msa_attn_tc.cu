@@ -73,13 +73,22 @@ __global__ void csr_count_kernel(AttnPass a) {
 }
 
 // Exclusive scans of entry counts and of tile counts, one CTA of 1024 threads.
+// Each thread owns a contiguous run of lists, read and written with 16-byte
+// accesses where the run is aligned.
 __global__ void __launch_bounds__(1024) csr_scan_kernel(AttnPass a) {
   __shared__ int64_t s_e[1024], s_t[1024];
   const int n = a.nlists;
-  const int per = (n + 1023) / 1024;
-  const int lo = threadIdx.x * per, hi = min(n, lo + per);
+  const int per = ((n + 1023) / 1024 + 3) & ~3;  // a multiple of 4
+  const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
   int64_t se = 0, st = 0;
-  for (int k = lo; k < hi; ++k) {
+  int k = lo;
+  for (; k + 4 <= hi; k += 4) {
+    const int4 c = *reinterpret_cast<const int4*>(a.count + k);
+    se += (int64_t)c.x + c.y + c.z + c.w;
+    st += (c.x + a.R - 1) / a.R + (c.y + a.R - 1) / a.R + (c.z + a.R - 1) / a.R +
+          (c.w + a.R - 1) / a.R;
+  }
+  for (; k < hi; ++k) {
     const int c = a.count[k];
     se += c;
     st += (c + a.R - 1) / a.R;
@@ -99,7 +108,18 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(AttnPass a) {
     __syncthreads();
   }
   int64_t oe = s_e[threadIdx.x] - se, ot = s_t[threadIdx.x] - st;
-  for (int k = lo; k < hi; ++k) {
+  k = lo;
+  for (; k + 4 <= hi; k += 4) {
+    const int4 c = *reinterpret_cast<const int4*>(a.count + k);
+    int4 o, t;
+    o.x = (int)oe; t.x = (int)ot; oe += c.x; ot += (c.x + a.R - 1) / a.R;
+    o.y = (int)oe; t.y = (int)ot; oe += c.y; ot += (c.y + a.R - 1) / a.R;
+    o.z = (int)oe; t.z = (int)ot; oe += c.z; ot += (c.z + a.R - 1) / a.R;
+    o.w = (int)oe; t.w = (int)ot; oe += c.w; ot += (c.w + a.R - 1) / a.R;
+    *reinterpret_cast<int4*>(a.off + k) = o;
+    *reinterpret_cast<int4*>(a.tile_off + k) = t;
+  }
+  for (; k < hi; ++k) {
     const int c = a.count[k];
     a.off[k] = (int32_t)oe;
     a.tile_off[k] = (int32_t)ot;

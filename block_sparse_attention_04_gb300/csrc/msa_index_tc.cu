@@ -33,7 +33,7 @@ namespace {
 
 constexpr int kTileRows = 128;
 constexpr int kItemRows = kTileRows;   // (query, group) rows per work item
-constexpr int kSplitBlocks = 512;
+constexpr int kSplitBlocks = 1024;
 constexpr int kPairKeys = 2 * kBlock;  // keys per MMA (N) and per accumulator stage
 constexpr int kStages = 4;             // K_idx stages (two key blocks each) in flight
 constexpr int kAccStages = 2;          // TMEM accumulator stages of kPairKeys columns
@@ -117,23 +117,6 @@ __device__ __forceinline__ void item_range(const IndexTcArgs& a, int32_t packed,
   p = (int)((uint32_t)packed >> 15);
   k0 = sp * kSplitBlocks;
   k1 = min(k0 + kSplitBlocks, pair_kb_end(a.s, a.pos, b, p));
-}
-
-// max of 128 fp32 values held as bits, as a tree of 3-input maxima
-__device__ __forceinline__ float max128(const uint32_t (&v)[128]) {
-  float l1[43];
-#pragma unroll
-  for (int k = 0; k < 42; ++k)
-    l1[k] = fmax3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]), __uint_as_float(v[3 * k + 2]));
-  l1[42] = fmaxf(__uint_as_float(v[126]), __uint_as_float(v[127]));
-  float l2[15];
-#pragma unroll
-  for (int k = 0; k < 14; ++k) l2[k] = fmax3(l1[3 * k], l1[3 * k + 1], l1[3 * k + 2]);
-  l2[14] = l1[42];
-  float l3[5];
-#pragma unroll
-  for (int k = 0; k < 5; ++k) l3[k] = fmax3(l2[3 * k], l2[3 * k + 1], l2[3 * k + 2]);
-  return fmax3(fmax3(l3[0], l3[1], l3[2]), l3[3], l3[4]);
 }
 
 // Insert (cs, ci) into a list sorted by (score desc, id asc) when ci is larger
