@@ -481,6 +481,74 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(
   }
 }
 
+// topk_merge for at most kSmallLists lists per row: one thread per (pass row,
+// group) keeps the head of every list in registers and takes the best head 15
+// times.  Same result as topk_merge_kernel; more rows in flight.
+constexpr int kSmallLists = 8;
+__global__ void __launch_bounds__(256) topk_merge_small_kernel(
+    Shape s, Positions pos, int T, int t0, int Tp, int bps, int nsplit, int nrows,
+    const Cand* __restrict__ cand, int32_t* __restrict__ sel) {
+  const int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gi >= (int64_t)nrows * s.G) return;
+  const int row = (int)(gi / s.G), g = (int)(gi % s.G);
+  const int b = row / Tp, i = t0 + row % Tp;
+  const int64_t t = (int64_t)pos.q_start[b] + i;
+  const int lb = (int)(t / kBlock);
+  const int nvalid = (lb + bps - 1) / bps;
+  const Cand* base = cand + (size_t)row * nsplit * s.G * kCand + (size_t)g * kCand;
+  const size_t lstride = (size_t)s.G * kCand;
+  float hs[kSmallLists];
+  int hi[kSmallLists], cur[kSmallLists];
+#pragma unroll
+  for (int k = 0; k < kSmallLists; ++k) {
+    cur[k] = 0;
+    hs[k] = -INFINITY;
+    hi[k] = INT_MAX;
+    if (k < nvalid) {
+      const Cand c = base[(size_t)k * lstride];
+      hs[k] = c.score;
+      hi[k] = c.id;
+    }
+  }
+  int keys[kTopk];
+#pragma unroll
+  for (int r = 0; r < kCand; ++r) {
+    int bk = 0;
+    float bs = hs[0];
+    int bid = hi[0];
+#pragma unroll
+    for (int k = 1; k < kSmallLists; ++k)
+      if (cand_better(hs[k], hi[k], bs, bid)) {
+        bs = hs[k];
+        bid = hi[k];
+        bk = k;
+      }
+    int wi = INT_MAX;
+#pragma unroll
+    for (int k = 0; k < kSmallLists; ++k) {
+      if (k == bk) {
+        wi = hi[k];
+        ++cur[k];
+        Cand c = Cand{-INFINITY, INT_MAX};
+        if (cur[k] < kCand && wi != INT_MAX) c = base[(size_t)k * lstride + cur[k]];
+        hs[k] = c.score;
+        hi[k] = c.id;
+      }
+    }
+    keys[r] = r < lb ? wi : INT_MAX;
+  }
+  keys[kCand] = lb;
+  // ascending ids, -1 padding last: each key goes to its rank
+  int32_t* out = sel + ((size_t)(b * T + i) * s.G + g) * kTopk;
+#pragma unroll
+  for (int j = 0; j < kTopk; ++j) {
+    int rank = 0;
+#pragma unroll
+    for (int k = 0; k < kTopk; ++k) rank += (keys[k] < keys[j]) || (keys[k] == keys[j] && k < j);
+    out[rank] = keys[j] == INT_MAX ? -1 : keys[j];
+  }
+}
+
 int pick_bps(int max_lb) {
   int bps = 64;
   while ((max_lb + bps - 1) / bps > kMaxSplits && bps < kMaxBps) bps *= 2;
@@ -539,9 +607,14 @@ cudaError_t launch_topk_merge(const Shape& s, const Positions& pos, int t0, int 
   const int rows = s.B * Tp;
   if (rows <= 0) return cudaSuccess;
   const int64_t warps = (int64_t)rows * s.G;
+  const int max_lb = max_local_block(s, pos, t0, t1);
   note_launches(1);
-  topk_merge_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(s, pos, s.T, t0, Tp, bps, nsplit,
-                                                               rows, cand, sel);
+  if ((max_lb + bps - 1) / bps <= kSmallLists)
+    topk_merge_small_kernel<<<(unsigned)((warps + 255) / 256), 256, 0, st>>>(
+        s, pos, s.T, t0, Tp, bps, nsplit, rows, cand, sel);
+  else
+    topk_merge_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(s, pos, s.T, t0, Tp, bps,
+                                                                 nsplit, rows, cand, sel);
   return cudaGetLastError();
 }
 
