@@ -11,10 +11,13 @@
 //   TMA           K and V of block kb, KV head g (block-major cache: 128 rows of
 //                 D bf16 at stride G*D)
 //   warps 0-3     gather the Q rows of the tile's entries into swizzled smem
-//   warp 8        tcgen05.mma  S = Q K^T (TMEM)  and  O = P V (TMEM, V MN-major)
+//   warp 8        tcgen05.mma  S = Q K^T (TMEM)  and  O = P V (P read from
+//                 TMEM, V an MN-major smem operand)
 //   warps 4-7     row softmax of S (block-local max m, sum l; causal mask on the
-//                 local block), P as bf16 into smem, then O/l as a bf16 partial
-// Each (query, head, slot) partial (O/l, m, l) is combined by a log-sum-exp
+//                 local block), P as bf16 written over S in TMEM, (m, l) out
+//   warps 9-12    O as an unnormalised bf16 partial, overlapping the next
+//                 tile's softmax
+// Each (query, head, slot) partial (O, m, l) is combined by a log-sum-exp
 // merge into the bf16 output.
 #include <climits>
 
@@ -25,7 +28,7 @@
 namespace msa {
 namespace {
 
-constexpr int kAttnThreads = 288;  // 9 warps
+constexpr int kAttnThreads = 416;  // 13 warps
 constexpr int kPassRows = 8192;    // (sequence, query) rows per pass
 
 struct AttnPass {
@@ -42,7 +45,7 @@ struct AttnPass {
   int32_t* tile_off;     // [nlists + 1]   tile offsets; tile_off[nlists] = total
   int32_t* entries;      // packed (i - t0) * 16 + slot
   int32_t* tile_list;    // list of each tile
-  uint16_t* part_o;      // [B*Tp*H*16][D] bf16, O / l
+  uint16_t* part_o;      // [B*Tp*H*16][D] bf16, O = sum 2^(s-m) v (unnormalised)
   float2* part_ml;       // [B*Tp*H*16] (m in log2 units, l)
   int* status;
 };
@@ -180,7 +183,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   using C = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t* sQ = smem;                       // Q, then P
+  uint8_t* sQ = smem;  // Q of the tile (P lives in TMEM)
   uint8_t* sK = smem + C::kSmemQ;
   uint8_t* sV = sK + C::kSmemK;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + C::kSmemV);
@@ -217,6 +220,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   const uint32_t tmem = *tmem_slot;
 
   const int H = a.s.H, G = a.s.G, hpg = H / G;
+  // r / hpg == (r * hpg_magic) >> 16 for every row r < 128 and hpg <= 128
+  const uint32_t hpg_magic = 65536u / (uint32_t)hpg + 1u;
   // a contiguous range of tiles per CTA: consecutive tiles of one list reuse
   // the K/V block already in shared memory
   const int ntiles = a.tile_off[a.nlists];
@@ -256,16 +261,28 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         for (int h = 0; h < C::kNHalf; ++h)
           tma_load_3d(smem_u32(sK + h * C::kHalf), &tm_k, bar_k, h * 64, g, row);
       }
-      // Q rows: row r = entry e * hpg + head hh; 16-byte chunks, swizzled
+      // Q rows: row r = entry e * hpg + head hh; 16-byte chunks, swizzled.
+      // Thread t copies chunk t % kChunks of rows t / kChunks + k * kRowStep.
+      // All row offsets are computed first, so the entry loads overlap.
       constexpr int kChunks = D / 8;
-      for (int c = threadIdx.x; c < nrows * kChunks; c += 128) {
-        const int r = c / kChunks, ch = c % kChunks;
-        const int e = r / hpg, hh = r - (r / hpg) * hpg;
-        const int il = ent[e] >> 4;
-        const uint16_t* src =
-            q + (((size_t)b * a.s.T + a.t0 + il) * H + (size_t)g * hpg + hh) * D + ch * 8;
-        cp_async_16(smem_u32(sQ + (ch >> 3) * C::kHalf + sw128(r, ch & 7)), src);
+      constexpr int kRowStep = 128 / kChunks;
+      const int ch = threadIdx.x % kChunks, r0 = threadIdx.x / kChunks;
+      const uint16_t* qb = q + (((size_t)b * a.s.T + a.t0) * H + (size_t)g * hpg) * D + ch * 8;
+      int rowoff[kChunks];
+#pragma unroll
+      for (int k = 0; k < kChunks; ++k) {
+        const int r = r0 + k * kRowStep;
+        rowoff[k] = -1;
+        if (r < nrows) {
+          const int e = (int)(((uint32_t)r * hpg_magic) >> 16);
+          rowoff[k] = (ent[e] >> 4) * H + (r - e * hpg);
+        }
       }
+#pragma unroll
+      for (int k = 0; k < kChunks; ++k)
+        if (rowoff[k] >= 0)
+          cp_async_16(smem_u32(sQ + (ch >> 3) * C::kHalf + sw128(r0 + k * kRowStep, ch & 7)),
+                      qb + (size_t)rowoff[k] * D);
       cp_async_commit();
       cp_async_wait<0>();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -281,12 +298,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       }
     } else if (warp == 8) {
       // -------------------------------------------------- MMA (warp 8)
+      // tcgen05.mma executes in issue order, so S of this tile cannot
+      // overwrite the P that the previous P.V still reads; P.V of this tile
+      // waits for the previous O to have been read out.
       bool ok = true;
       if (lane == 0) {
         constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
         constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
-        ok = mbar_wait(bar_q, ph, a.status) && mbar_wait(bar_k, kv_ph, a.status) &&
-             (it == 0 || mbar_wait(bar_done, ph ^ 1, a.status));
+        ok = mbar_wait(bar_q, ph, a.status) && mbar_wait(bar_k, kv_ph, a.status);
         if (ok) {
           tc_fence_after();
           const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
@@ -297,7 +316,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                        smem_desc(k0 + off, 16, 1024, kSwizzle128B), idesc_s, k > 0);
           }
           tc_commit(bar_s);
-          ok = mbar_wait(bar_p, ph, a.status) && mbar_wait(bar_v, kv_ph, a.status);
+          ok = mbar_wait(bar_p, ph, a.status) && mbar_wait(bar_v, kv_ph, a.status) &&
+               (it == 0 || mbar_wait(bar_done, ph ^ 1, a.status));
           if (ok) {
             tc_fence_after();
             // P (bf16, two per column) is in TMEM columns [0, 64): 8 per 16 tokens
@@ -310,12 +330,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         }
       }
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { *abort_flag = 1; break; }
-    } else {
+    } else if (warp < 8) {
       // -------------------------------------------------- softmax (warps 4-7)
       const int quad = warp & 3;
       const int r = quad * 32 + lane;  // tile row = TMEM lane
-      const bool valid = r < nrows;
       int il = 0, hh = 0, slot = 0;
+      const bool valid = r < nrows;
       if (valid) {
         const int e = r / hpg;
         hh = r - e * hpg;
@@ -325,25 +345,51 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       const int64_t t = (int64_t)a.pos.q_start[b] + a.t0 + il;
       // tokens kb*128 + c with c > lim are masked (only in the local block)
       const int lim = (int)(t - (int64_t)kb * kBlock);
+      const bool masked = __any_sync(0xffffffffu, valid && lim < kBlock - 1);
       if (!__all_sync(0xffffffffu, mbar_wait(bar_s, ph, a.status))) { *abort_flag = 1; break; }
       tc_fence_after();
       const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
       const float sl = a.s.scale * kLog2e;
       uint32_t v[32];
-      // pass 1: row max of the scaled, masked scores
-      float m = -INFINITY;
+      // pass 1: row maximum of the scaled scores (maximum or minimum of the
+      // raw scores, by the sign of the scale)
+      float mx = -INFINITY, mn = INFINITY;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(lane_base + c * 32, v);
         tmem_ld_wait();
+        if (masked) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (c * 32 + e <= lim) m = fmaxf(m, __uint_as_float(v[e]) * sl);
+          for (int e = 0; e < 32; ++e) {
+            const float x = __uint_as_float(v[e]);
+            const bool in = c * 32 + e <= lim;
+            mx = fmaxf(mx, in ? x : -INFINITY);
+            mn = fminf(mn, in ? x : INFINITY);
+          }
+        } else {
+          float t3[11], u3[11];
+#pragma unroll
+          for (int k = 0; k < 10; ++k) {
+            t3[k] = fmax3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]),
+                          __uint_as_float(v[3 * k + 2]));
+            u3[k] = fmin3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]),
+                          __uint_as_float(v[3 * k + 2]));
+          }
+          t3[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+          u3[10] = fminf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+          mx = fmax3(mx, fmax3(fmax3(t3[0], t3[1], t3[2]), fmax3(t3[3], t3[4], t3[5]),
+                               fmax3(t3[6], t3[7], t3[8])),
+                     fmaxf(t3[9], t3[10]));
+          mn = fmin3(mn, fmin3(fmin3(u3[0], u3[1], u3[2]), fmin3(u3[3], u3[4], u3[5]),
+                               fmin3(u3[6], u3[7], u3[8])),
+                     fminf(u3[9], u3[10]));
+        }
       }
-      // pass 2: P = 2^(s - m) as bf16, two per column, written over S in TMEM
-      // (chunk c of S is read before columns [16c, 16c+16) are written, and
-      // those columns belong to chunks already read); row sum
-      float l = 0.f;
+      const float m = sl >= 0.f ? mx * sl : mn * sl;
+      // pass 2: P = 2^(s*scale*log2e - m) as bf16, two per column, written
+      // over S in TMEM (chunk c of S is read before columns [16c, 16c+16) are
+      // written, and those columns belong to chunks already read); row sum
+      float l0 = 0.f, l1 = 0.f;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(lane_base + c * 32, v);
@@ -352,9 +398,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int e = 2 * u;
-          const float p0 = (c * 32 + e <= lim) ? ex2(__uint_as_float(v[e]) * sl - m) : 0.f;
-          const float p1 = (c * 32 + e + 1 <= lim) ? ex2(__uint_as_float(v[e + 1]) * sl - m) : 0.f;
-          l += p0 + p1;
+          float p0 = ex2(fmaf(__uint_as_float(v[e]), sl, -m));
+          float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl, -m));
+          if (masked) {
+            p0 = c * 32 + e <= lim ? p0 : 0.f;
+            p1 = c * 32 + e + 1 <= lim ? p1 : 0.f;
+          }
+          l0 += p0;
+          l1 += p1;
           w[u] = pack_bf16(p0, p1);
         }
         tmem_st16(lane_base + c * 16, w);
@@ -362,30 +413,49 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_p);
+      if (valid) {
+        const size_t prow = (((size_t)b * a.Tp + il) * H + (size_t)g * hpg + hh) * kTopk + slot;
+        __stcs(a.part_ml + prow, make_float2(m, l0 + l1));
+      }
+    } else {
+      // -------------------------------------------- O epilogue (warps 9-12)
+      // O = P.V (unnormalised) as a bf16 partial; the merge divides by the
+      // combined sum.  Runs while the softmax warps work on the next tile.
+      const int quad = warp & 3;
+      const int r = quad * 32 + lane;
+      const bool valid = r < nrows;
+      size_t prow = 0;
+      if (valid) {
+        const int e = r / hpg;
+        const int hh = r - e * hpg;
+        const int il = ent[e] >> 4;
+        prow = (((size_t)b * a.Tp + il) * H + (size_t)g * hpg + hh) * kTopk + (ent[e] & 15);
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(bar_o, ph, a.status))) { *abort_flag = 1; break; }
       tc_fence_after();
-      const float inv = 1.f / l;
-      const size_t prow = (((size_t)b * a.Tp + il) * H + (size_t)g * hpg + hh) * kTopk + slot;
+      const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + 128;
       uint16_t* dst = a.part_o + prow * D;
+      uint32_t v[32];
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(lane_base + 128 + c * 32, v);
+        tmem_ld32(lane_base + c * 32, v);
         tmem_ld_wait();
         if (valid) {
 #pragma unroll
           for (int e8 = 0; e8 < 4; ++e8) {
             uint4 pk;
-            pk.x = pack_bf16(__uint_as_float(v[e8 * 8 + 0]) * inv, __uint_as_float(v[e8 * 8 + 1]) * inv);
-            pk.y = pack_bf16(__uint_as_float(v[e8 * 8 + 2]) * inv, __uint_as_float(v[e8 * 8 + 3]) * inv);
-            pk.z = pack_bf16(__uint_as_float(v[e8 * 8 + 4]) * inv, __uint_as_float(v[e8 * 8 + 5]) * inv);
-            pk.w = pack_bf16(__uint_as_float(v[e8 * 8 + 6]) * inv, __uint_as_float(v[e8 * 8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(dst + c * 32 + e8 * 8) = pk;
+            pk.x = pack_bf16(__uint_as_float(v[e8 * 8 + 0]), __uint_as_float(v[e8 * 8 + 1]));
+            pk.y = pack_bf16(__uint_as_float(v[e8 * 8 + 2]), __uint_as_float(v[e8 * 8 + 3]));
+            pk.z = pack_bf16(__uint_as_float(v[e8 * 8 + 4]), __uint_as_float(v[e8 * 8 + 5]));
+            pk.w = pack_bf16(__uint_as_float(v[e8 * 8 + 6]), __uint_as_float(v[e8 * 8 + 7]));
+            // streaming store: the partial is read once, by the merge, and
+            // should not push Q and K/V out of L2
+            __stcs(reinterpret_cast<uint4*>(dst + c * 32 + e8 * 8), pk);
           }
         }
       }
       tc_fence_before();
       mbar_arrive(bar_done);
-      if (valid) a.part_ml[prow] = make_float2(m, l);
     }
   }
 
@@ -419,7 +489,7 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnPass a, uint16_t
   if (lane < kTopk) {
     const int kb = a.sel[(((size_t)b * a.s.T + i) * a.s.G + g) * kTopk + lane];
     if (slot_valid(a, b, i, kb)) {
-      const float2 ml = a.part_ml[prow0 + lane];
+      const float2 ml = __ldcs(a.part_ml + prow0 + lane);
       m = ml.x;
       l = ml.y;
     }
@@ -427,8 +497,10 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnPass a, uint16_t
   float M = m;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  const float w = (m == -INFINITY) ? 0.f : ex2(m - M) * l;
-  float W = w;
+  // partial j holds O_j = sum p v with p = 2^(s - m_j): weight 2^(m_j - M),
+  // normaliser sum_j 2^(m_j - M) l_j
+  const float w = (m == -INFINITY) ? 0.f : ex2(m - M);
+  float W = w * l;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
   float acc[PER];
@@ -439,13 +511,13 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnPass a, uint16_t
     if (wj == 0.f) continue;
     const uint16_t* src = a.part_o + (prow0 + j) * D + lane * PER;
     if constexpr (PER == 4) {
-      const uint2 u = *reinterpret_cast<const uint2*>(src);
+      const uint2 u = __ldcs(reinterpret_cast<const uint2*>(src));
       acc[0] += wj * bf16lo(u.x);
       acc[1] += wj * bf16hi(u.x);
       acc[2] += wj * bf16lo(u.y);
       acc[3] += wj * bf16hi(u.y);
     } else {
-      const uint32_t u = *reinterpret_cast<const uint32_t*>(src);
+      const uint32_t u = __ldcs(reinterpret_cast<const unsigned int*>(src));
       acc[0] += wj * bf16lo(u);
       acc[1] += wj * bf16hi(u);
     }

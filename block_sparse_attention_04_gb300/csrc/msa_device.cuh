@@ -19,8 +19,18 @@ __device__ __forceinline__ uint32_t f32_to_bf16_rne(float x) {
   return u >> 16;
 }
 
+// Two fp32 -> bf16 (round to nearest even) in one conversion: `lo` in bits
+// 0-15, `hi` in bits 16-31.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  return f32_to_bf16_rne(lo) | (f32_to_bf16_rne(hi) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
