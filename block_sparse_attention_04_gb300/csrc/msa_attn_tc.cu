@@ -44,7 +44,7 @@ struct AttnPass {
   int32_t* off;          // [nlists + 1]   entry offsets
   int32_t* tile_off;     // [nlists + 1]   tile offsets; tile_off[nlists] = total
   int32_t* entries;      // packed (i - t0) * 16 + slot
-  int32_t* tile_list;    // list of each tile
+  int4* tile_desc;       // per tile: list, first entry, entries, kb | g << 15 | b << 18
   uint16_t* part_o;      // [B*Tp*H*16][D] bf16, O = sum 2^(s-m) v (unnormalised)
   float2* part_ml;       // [B*Tp*H*16] (m in log2 units, l)
   int* status;
@@ -150,11 +150,18 @@ __global__ void csr_fill_kernel(AttnPass a) {
     const int p = atomicAdd(&a.cursor[L], 1);
     a.entries[a.off[L] + p] = il * kTopk + j;
   }
-  // tile table: thread per list
+  // tile table, thread per list: one 16-byte descriptor per tile, so the
+  // attention kernel reads a tile's coordinates with a single load
   for (int64_t L = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; L < a.nlists;
        L += (int64_t)gridDim.x * blockDim.x) {
     const int t0 = a.tile_off[L], t1 = a.tile_off[L + 1];
-    for (int k = t0; k < t1; ++k) a.tile_list[k] = (int32_t)L;
+    if (t0 == t1) continue;
+    const int g = (int)(L % a.s.G), kb = (int)((L / a.s.G) % a.nbl), b = (int)(L / (a.s.G * a.nbl));
+    const int cnt = a.count[L], o = a.off[L];
+    for (int k = t0; k < t1; ++k) {
+      const int e0 = (k - t0) * a.R;
+      a.tile_desc[k] = make_int4((int)L, o + e0, min(a.R, cnt - e0), kb | (g << 15) | (b << 18));
+    }
   }
 }
 
@@ -174,6 +181,28 @@ struct AttnCfg {
 // with the 128-byte swizzle (chunk index XOR row mod 8).
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// Maximum / minimum of 32 fp32 values held as raw bits (3-input trees).
+__device__ __forceinline__ float tree_max32(const uint32_t (&v)[32]) {
+  float t[11];
+#pragma unroll
+  for (int k = 0; k < 10; ++k)
+    t[k] = fmax3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]),
+                 __uint_as_float(v[3 * k + 2]));
+  t[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+  return fmax3(fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], t[8])),
+               t[9], t[10]);
+}
+__device__ __forceinline__ float tree_min32(const uint32_t (&v)[32]) {
+  float t[11];
+#pragma unroll
+  for (int k = 0; k < 10; ++k)
+    t[k] = fmin3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]),
+                 __uint_as_float(v[3 * k + 2]));
+  t[10] = fminf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+  return fmin3(fmin3(fmin3(t[0], t[1], t[2]), fmin3(t[3], t[4], t[5]), fmin3(t[6], t[7], t[8])),
+               t[9], t[10]);
 }
 
 template <int D>
@@ -231,21 +260,23 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   uint32_t it = 0;      // tiles processed by this CTA (phase of the per-tile barriers)
   uint32_t kv_it = 0;   // K/V loads issued by this CTA (phase of bar_k, bar_v)
   int prev_list = -1;
+  // the next tile's descriptor is loaded one iteration ahead
+  int4 dnext = tile_lo < tile_hi ? a.tile_desc[tile_lo] : make_int4(0, 0, 0, 0);
   for (int tile = tile_lo; tile < tile_hi; ++tile, ++it) {
     if (*abort_flag) break;
     const uint32_t ph = it & 1;
-    const int L = a.tile_list[tile];
+    const int4 d = dnext;
+    if (tile + 1 < tile_hi) dnext = a.tile_desc[tile + 1];
+    const int L = d.x;
     const bool reuse_kv = (L == prev_list);
     prev_list = L;
     const uint32_t kv_ph = reuse_kv ? ((kv_it - 1) & 1) : (kv_it & 1);
     if (!reuse_kv) ++kv_it;
-    const int g = L % G;
-    const int kb = (L / G) % a.nbl;
-    const int b = L / (G * a.nbl);
-    const int e0 = (tile - a.tile_off[L]) * a.R;
-    const int ne = min(a.R, a.count[L] - e0);
-    const int32_t* ent = a.entries + a.off[L] + e0;
-    const int nrows = ne * hpg;
+    const int kb = d.w & 0x7FFF;
+    const int g = (d.w >> 15) & 7;
+    const int b = d.w >> 18;
+    const int32_t* ent = a.entries + d.y;
+    const int nrows = d.z * hpg;
 
     if (warp < 4) {
       // -------------------------------------------------- loads (warps 0-3)
@@ -351,9 +382,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
       const float sl = a.s.scale * kLog2e;
       uint32_t v[32];
-      // pass 1: row maximum of the scaled scores (maximum or minimum of the
-      // raw scores, by the sign of the scale)
-      float mx = -INFINITY, mn = INFINITY;
+      // pass 1: row maximum of the scaled scores: the maximum of the raw
+      // scores, or their minimum when the scale is negative
+      const bool neg = sl < 0.f;
+      float mx = neg ? INFINITY : -INFINITY;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(lane_base + c * 32, v);
@@ -363,29 +395,15 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           for (int e = 0; e < 32; ++e) {
             const float x = __uint_as_float(v[e]);
             const bool in = c * 32 + e <= lim;
-            mx = fmaxf(mx, in ? x : -INFINITY);
-            mn = fminf(mn, in ? x : INFINITY);
+            mx = neg ? fminf(mx, in ? x : INFINITY) : fmaxf(mx, in ? x : -INFINITY);
           }
+        } else if (!neg) {
+          mx = fmax3(mx, tree_max32(v), -INFINITY);
         } else {
-          float t3[11], u3[11];
-#pragma unroll
-          for (int k = 0; k < 10; ++k) {
-            t3[k] = fmax3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]),
-                          __uint_as_float(v[3 * k + 2]));
-            u3[k] = fmin3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]),
-                          __uint_as_float(v[3 * k + 2]));
-          }
-          t3[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
-          u3[10] = fminf(__uint_as_float(v[30]), __uint_as_float(v[31]));
-          mx = fmax3(mx, fmax3(fmax3(t3[0], t3[1], t3[2]), fmax3(t3[3], t3[4], t3[5]),
-                               fmax3(t3[6], t3[7], t3[8])),
-                     fmaxf(t3[9], t3[10]));
-          mn = fmin3(mn, fmin3(fmin3(u3[0], u3[1], u3[2]), fmin3(u3[3], u3[4], u3[5]),
-                               fmin3(u3[6], u3[7], u3[8])),
-                     fminf(u3[9], u3[10]));
+          mx = fmin3(mx, tree_min32(v), INFINITY);
         }
       }
-      const float m = sl >= 0.f ? mx * sl : mn * sl;
+      const float m = mx * sl;
       // pass 2: P = 2^(s*scale*log2e - m) as bf16, two per column, written
       // over S in TMEM (chunk c of S is read before columns [16c, 16c+16) are
       // written, and those columns belong to chunks already read); row sum
@@ -546,7 +564,7 @@ AttnLayout attn_layout(const Shape& s) {
   L.off_off = o;    o += al((L.lists + 1) * 4);
   L.toff_off = o;   o += al((L.lists + 1) * 4);
   L.ent_off = o;    o += al(L.entries * 4);
-  L.tl_off = o;     o += al(L.entries * 4);
+  L.tl_off = o;     o += al(L.entries * 16);
   const size_t prows = (size_t)s.B * tp * s.H * kTopk;
   L.po_off = o;     o += al(prows * s.D * 2);
   L.pml_off = o;    o += al(prows * 8);
@@ -597,7 +615,7 @@ cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint
     a.off = reinterpret_cast<int32_t*>(base + lay.off_off);
     a.tile_off = reinterpret_cast<int32_t*>(base + lay.toff_off);
     a.entries = reinterpret_cast<int32_t*>(base + lay.ent_off);
-    a.tile_list = reinterpret_cast<int32_t*>(base + lay.tl_off);
+    a.tile_desc = reinterpret_cast<int4*>(base + lay.tl_off);
     a.part_o = reinterpret_cast<uint16_t*>(base + lay.po_off);
     a.part_ml = reinterpret_cast<float2*>(base + lay.pml_off);
     a.status = ws.status;
