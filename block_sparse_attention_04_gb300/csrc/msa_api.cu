@@ -30,8 +30,9 @@ int validate_params(const msa_params* p) {
   if (p->Di != 32 && p->Di != 64) return MSA_ERR_UNSUPPORTED;
   if (p->G > 8 || p->H / p->G > 16) return MSA_ERR_UNSUPPORTED;
   if (p->max_blocks > kMaxContextBlocks) return MSA_ERR_UNSUPPORTED;
-  // TMA coordinates are 32-bit: rows of q_idx and of k_idx must fit
+  // TMA coordinates are 32-bit: rows of q_idx, q (one per head) and k_idx must fit
   if ((int64_t)p->B * p->T * p->G >= ((int64_t)1 << 31) ||
+      (int64_t)p->B * p->T * p->H >= ((int64_t)1 << 31) ||
       (int64_t)p->B * p->max_blocks * MSA_BLOCK >= ((int64_t)1 << 31))
     return MSA_ERR_UNSUPPORTED;
   return MSA_OK;

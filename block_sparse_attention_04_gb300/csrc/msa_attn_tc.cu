@@ -28,7 +28,7 @@
 namespace msa {
 namespace {
 
-constexpr int kAttnThreads = 416;  // 13 warps
+constexpr int kAttnThreads = 320;  // 10 warps
 constexpr int kPassRows = 8192;    // (sequence, query) rows per pass
 
 struct AttnPass {
@@ -37,7 +37,8 @@ struct AttnPass {
   int t0, Tp;            // queries [t0, t0+Tp) of every sequence
   int nbl;               // key blocks per (sequence, group) in the list space
   int nlists;            // B * nbl * G
-  int R;                 // entries per tile = 128 / (H/G)
+  int R;                 // entries per tile = 128 / rpe
+  int rpe;               // tile rows per entry: H/G rounded up to 8 or 16
   const int32_t* sel;    // [B][T][G][16]
   int32_t* count;        // [nlists]
   int32_t* cursor;       // [nlists]
@@ -177,12 +178,6 @@ struct AttnCfg {
   static constexpr uint32_t kTmemCols = 256;            // S [0,128) and O [128, 128+D)
 };
 
-// Byte offset of 16-byte chunk `c` (0..7) of row `r` in a [128][64] bf16 box
-// with the 128-byte swizzle (chunk index XOR row mod 8).
-__device__ __forceinline__ uint32_t sw128(int r, int c) {
-  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
-}
-
 // Maximum / minimum of 32 fp32 values held as raw bits (3-input trees).
 __device__ __forceinline__ float tree_max32(const uint32_t (&v)[32]) {
   float t[11];
@@ -207,8 +202,8 @@ __device__ __forceinline__ float tree_min32(const uint32_t (&v)[32]) {
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 2)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                   const uint16_t* __restrict__ q, const AttnPass a) {
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const AttnPass a) {
   using C = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -231,7 +226,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   if (threadIdx.x == 0) {
     mbar_init(bar_k, 1);
     mbar_init(bar_v, 1);
-    mbar_init(bar_q, 128);
+    mbar_init(bar_q, 1);
     mbar_init(bar_s, 1);
     mbar_init(bar_p, 128);
     mbar_init(bar_o, 1);
@@ -239,18 +234,18 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     mbar_init(bar_fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
-  if (warp == 8) tmem_alloc(tmem_slot, C::kTmemCols);
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int H = a.s.H, G = a.s.G, hpg = H / G;
-  // r / hpg == (r * hpg_magic) >> 16 for every row r < 128 and hpg <= 128
-  const uint32_t hpg_magic = 65536u / (uint32_t)hpg + 1u;
+  const int H = a.s.H, hpg = H / a.s.G;
+  const int rshift = a.rpe == 8 ? 3 : 4;  // tile row -> entry
   // a contiguous range of tiles per CTA: consecutive tiles of one list reuse
   // the K/V block already in shared memory
   const int ntiles = a.tile_off[a.nlists];
@@ -260,6 +255,22 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   uint32_t it = 0;      // tiles processed by this CTA (phase of the per-tile barriers)
   uint32_t kv_it = 0;   // K/V loads issued by this CTA (phase of bar_k, bar_v)
   int prev_list = -1;
+  // Q boxes are 8 rows (heads) x 64 dims, one 128-byte-swizzle atom each:
+  // an entry takes rpe/8 boxes per 64-dim half, a tile at most 32 boxes, so
+  // lane j copies box j (entry-major, then half, then 8-row group).
+  const int bpe = a.rpe >> 3;                   // boxes per entry and half
+  const int box_e = lane / (bpe * C::kNHalf);   // this lane's entry
+  const int box_h = (lane / bpe) % C::kNHalf;   // its 64-dim half
+  const int box_r = (lane % bpe) * 8;           // its first row within the entry
+  // row of q (token * H + head) where this lane's box starts, for a tile;
+  // loaded one tile ahead
+  auto q_row = [&](const int4& dd) -> int {
+    if (box_e >= dd.z) return 0;
+    const int il = a.entries[dd.y + box_e] >> 4;
+    return (int)((((int64_t)(dd.w >> 18) * a.s.T + a.t0 + il) * H) + ((dd.w >> 15) & 7) * hpg +
+                 box_r);
+  };
+  int qrow = 0;
   // the next tile's descriptor is loaded one iteration ahead
   int4 dnext = tile_lo < tile_hi ? a.tile_desc[tile_lo] : make_int4(0, 0, 0, 0);
   for (int tile = tile_lo; tile < tile_hi; ++tile, ++it) {
@@ -275,60 +286,50 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     const int kb = d.w & 0x7FFF;
     const int g = (d.w >> 15) & 7;
     const int b = d.w >> 18;
+    const int ne = d.z;
     const int32_t* ent = a.entries + d.y;
-    const int nrows = d.z * hpg;
 
-    if (warp < 4) {
-      // -------------------------------------------------- loads (warps 0-3)
+    if (warp == 0) {
+      // ------------------------------------------------------ TMA (warp 0)
       // Q and K of this tile once S of the previous tile is done (P lives in
-      // TMEM, so the Q buffer is free then); V once its P.V is done.
+      // TMEM, so the Q buffer is free then); V once its P.V is done.  Entry e
+      // fills tile rows [e*rpe, e*rpe + rpe): its hpg heads, then heads of the
+      // next group or token (or zero fill past the end), which land in rows
+      // the softmax and epilogue skip.
+      if (tile == tile_lo) qrow = q_row(d);
       if (it > 0) {
         if (!__all_sync(0xffffffffu, mbar_wait(bar_s, ph ^ 1, a.status))) { *abort_flag = 1; break; }
       }
       const int row = (int)(((int64_t)b * a.s.max_blocks + kb) * kBlock);
-      if (warp == 0 && lane == 0 && !reuse_kv) {
-        mbar_arrive_expect_tx(bar_k, C::kNHalf * C::kHalf);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_q, (uint32_t)(ne * a.rpe * D * 2));
+        if (!reuse_kv) {
+          mbar_arrive_expect_tx(bar_k, C::kNHalf * C::kHalf);
 #pragma unroll
-        for (int h = 0; h < C::kNHalf; ++h)
-          tma_load_3d(smem_u32(sK + h * C::kHalf), &tm_k, bar_k, h * 64, g, row);
-      }
-      // Q rows: row r = entry e * hpg + head hh; 16-byte chunks, swizzled.
-      // Thread t copies chunk t % kChunks of rows t / kChunks + k * kRowStep.
-      // All row offsets are computed first, so the entry loads overlap.
-      constexpr int kChunks = D / 8;
-      constexpr int kRowStep = 128 / kChunks;
-      const int ch = threadIdx.x % kChunks, r0 = threadIdx.x / kChunks;
-      const uint16_t* qb = q + (((size_t)b * a.s.T + a.t0) * H + (size_t)g * hpg) * D + ch * 8;
-      int rowoff[kChunks];
-#pragma unroll
-      for (int k = 0; k < kChunks; ++k) {
-        const int r = r0 + k * kRowStep;
-        rowoff[k] = -1;
-        if (r < nrows) {
-          const int e = (int)(((uint32_t)r * hpg_magic) >> 16);
-          rowoff[k] = (ent[e] >> 4) * H + (r - e * hpg);
+          for (int h = 0; h < C::kNHalf; ++h)
+            tma_load_3d(smem_u32(sK + h * C::kHalf), &tm_k, bar_k, h * 64, g, row);
         }
       }
-#pragma unroll
-      for (int k = 0; k < kChunks; ++k)
-        if (rowoff[k] >= 0)
-          cp_async_16(smem_u32(sQ + (ch >> 3) * C::kHalf + sw128(r0 + k * kRowStep, ch & 7)),
-                      qb + (size_t)rowoff[k] * D);
-      cp_async_commit();
-      cp_async_wait<0>();
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(bar_q);
-      if (it > 0) {
+      __syncwarp();
+      if (box_e < ne)
+        tma_load_2d(smem_u32(sQ + box_h * C::kHalf + (box_e * a.rpe + box_r) * 128), &tm_q, bar_q,
+                    box_h * 64, qrow);
+      if (tile + 1 < tile_hi) qrow = q_row(dnext);
+      // V only for a new list.  The wait for the previous P.V happens only
+      // then: a tile that reuses K/V needs nothing more from this warp, so its
+      // own P.V may complete meanwhile, and a parity wait on a barrier two
+      // phases ahead would never return.
+      if (it > 0 && !reuse_kv) {
         if (!__all_sync(0xffffffffu, mbar_wait(bar_o, ph ^ 1, a.status))) { *abort_flag = 1; break; }
       }
-      if (warp == 0 && lane == 0 && !reuse_kv) {
+      if (lane == 0 && !reuse_kv) {
         mbar_arrive_expect_tx(bar_v, C::kNHalf * C::kHalf);
 #pragma unroll
         for (int h = 0; h < C::kNHalf; ++h)
           tma_load_3d(smem_u32(sV + h * C::kHalf), &tm_v, bar_v, h * 64, g, row);
       }
-    } else if (warp == 8) {
-      // -------------------------------------------------- MMA (warp 8)
+    } else if (warp == 1) {
+      // -------------------------------------------------- MMA (warp 1)
       // tcgen05.mma executes in issue order, so S of this tile cannot
       // overwrite the P that the previous P.V still reads; P.V of this tile
       // waits for the previous O to have been read out.
@@ -361,15 +362,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         }
       }
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { *abort_flag = 1; break; }
-    } else if (warp < 8) {
-      // -------------------------------------------------- softmax (warps 4-7)
+    } else if (warp < 6) {
+      // -------------------------------------------------- softmax (warps 2-5)
       const int quad = warp & 3;
       const int r = quad * 32 + lane;  // tile row = TMEM lane
-      int il = 0, hh = 0, slot = 0;
-      const bool valid = r < nrows;
+      const int e = r >> rshift, hh = r & (a.rpe - 1);
+      const bool valid = e < ne && hh < hpg;
+      int il = 0, slot = 0;
       if (valid) {
-        const int e = r / hpg;
-        hh = r - e * hpg;
         il = ent[e] >> 4;
         slot = ent[e] & 15;
       }
@@ -392,9 +392,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         tmem_ld_wait();
         if (masked) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float x = __uint_as_float(v[e]);
-            const bool in = c * 32 + e <= lim;
+          for (int k = 0; k < 32; ++k) {
+            const float x = __uint_as_float(v[k]);
+            const bool in = c * 32 + k <= lim;
             mx = neg ? fminf(mx, in ? x : INFINITY) : fmaxf(mx, in ? x : -INFINITY);
           }
         } else if (!neg) {
@@ -415,12 +415,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         uint32_t w[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const int e = 2 * u;
-          float p0 = ex2(fmaf(__uint_as_float(v[e]), sl, -m));
-          float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl, -m));
+          const int k = 2 * u;
+          float p0 = ex2(fmaf(__uint_as_float(v[k]), sl, -m));
+          float p1 = ex2(fmaf(__uint_as_float(v[k + 1]), sl, -m));
           if (masked) {
-            p0 = c * 32 + e <= lim ? p0 : 0.f;
-            p1 = c * 32 + e + 1 <= lim ? p1 : 0.f;
+            p0 = c * 32 + k <= lim ? p0 : 0.f;
+            p1 = c * 32 + k + 1 <= lim ? p1 : 0.f;
           }
           l0 += p0;
           l1 += p1;
@@ -436,18 +436,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         __stcs(a.part_ml + prow, make_float2(m, l0 + l1));
       }
     } else {
-      // -------------------------------------------- O epilogue (warps 9-12)
+      // -------------------------------------------- O epilogue (warps 6-9)
       // O = P.V (unnormalised) as a bf16 partial; the merge divides by the
       // combined sum.  Runs while the softmax warps work on the next tile.
       const int quad = warp & 3;
       const int r = quad * 32 + lane;
-      const bool valid = r < nrows;
+      const int e = r >> rshift, hh = r & (a.rpe - 1);
+      const bool valid = e < ne && hh < hpg;
       size_t prow = 0;
       if (valid) {
-        const int e = r / hpg;
-        const int hh = r - e * hpg;
-        const int il = ent[e] >> 4;
-        prow = (((size_t)b * a.Tp + il) * H + (size_t)g * hpg + hh) * kTopk + (ent[e] & 15);
+        const int en = ent[e];
+        prow = (((size_t)b * a.Tp + (en >> 4)) * H + (size_t)g * hpg + hh) * kTopk + (en & 15);
       }
       if (!__all_sync(0xffffffffu, mbar_wait(bar_o, ph, a.status))) { *abort_flag = 1; break; }
       tc_fence_after();
@@ -478,13 +477,13 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   }
 
   // all MMAs done before TMEM is released
-  if (warp == 8 && lane == 0) {
+  if (warp == 1 && lane == 0) {
     tc_commit(bar_fin);
     mbar_wait(bar_fin, 0, nullptr);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -579,7 +578,17 @@ cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint
   using C = AttnCfg<D>;
   const AttnLayout lay = attn_layout(s);
   char* base = ws.tc_base;
-  CUtensorMap tm_k, tm_v;
+  const int hpg = s.H / s.G;
+  const int rpe = hpg <= 8 ? 8 : 16;
+  CUtensorMap tm_q, tm_k, tm_v;
+  {
+    // q as [B*T*H rows][D]: one box = 8 rows (heads) x 64 dims
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)s.B * s.T * s.H};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, 8};
+    if (!encode_bf16_map(&tm_q, q, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)s.G,
                           (cuuint64_t)s.B * s.max_blocks * kBlock};
@@ -598,7 +607,6 @@ cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint
   cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   const int grid = 2 * sm_count();
   const int tp_max = pass_len(s);
-  const int hpg = s.H / s.G;
   for (int t0 = 0; t0 < s.T; t0 += tp_max) {
     AttnPass a;
     a.s = s;
@@ -608,7 +616,8 @@ cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint
     const int max_lb = max_local_block(s, pos, t0, t0 + a.Tp);
     a.nbl = max_lb + 1;
     a.nlists = s.B * a.nbl * s.G;
-    a.R = 128 / hpg;
+    a.rpe = rpe;
+    a.R = 128 / rpe;
     a.sel = sel;
     a.count = reinterpret_cast<int32_t*>(base + lay.count_off);
     a.cursor = reinterpret_cast<int32_t*>(base + lay.cursor_off);
@@ -627,7 +636,7 @@ cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint
     csr_count_kernel<<<g1, 256, 0, st>>>(a);
     csr_scan_kernel<<<1, 1024, 0, st>>>(a);
     csr_fill_kernel<<<g1, 256, 0, st>>>(a);
-    attn_tc_kernel<D><<<grid, kAttnThreads, C::kSmem, st>>>(tm_k, tm_v, q, a);
+    attn_tc_kernel<D><<<grid, kAttnThreads, C::kSmem, st>>>(tm_q, tm_k, tm_v, a);
     const int64_t warps = (int64_t)s.B * a.Tp * s.H;
     note_launches(1);
     attn_tc_merge_kernel<D><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(a, out);

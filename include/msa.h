@@ -45,7 +45,9 @@
  *     whose bounded wait runs out records MSA_ERR_TIMEOUT in ws; read it with
  *     msa_workspace_status().
  *   - Supported shapes: block == 128, topk == 16, H % G == 0, D in {64, 128},
- *     Di in {32, 64}, 1 <= B <= MSA_MAX_BATCH, T >= 0 (T == 0 is a no-op).
+ *     Di in {32, 64}, 1 <= B <= MSA_MAX_BATCH, T >= 0 (T == 0 is a no-op),
+ *     G <= 8, H/G <= 16, max_blocks <= 32768, and B*T*H and
+ *     B*max_blocks*128 below 2^31 (tensor-copy row coordinates are 32-bit).
  *     Others return MSA_ERR_UNSUPPORTED.
  *   - Pointers must be 16-byte aligned (MSA_ERR_INVALID_ARG otherwise).
  */

@@ -63,6 +63,19 @@ def test_prefill_m2_layout_ragged_tail(msa, ref, kernels):
     assert_close(out, want_out)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("H,G", [(4, 4), (8, 4), (12, 4), (20, 4), (48, 8), (28, 4), (32, 4),
+                                 (40, 4), (48, 4), (64, 4), (16, 1)])
+def test_head_layouts_on_tensor_cores(msa, ref, H, G, D):
+    # heads per group 1..16: the KV-outer tiles hold whole groups of heads per
+    # query, padded to 8 or 16 rows, and copy them as 8-row boxes
+    wl = Workload(B=1, T=700, H=H, G=G, D=D, Di=64, ctx=[700 + 1300], q_start=[1300])
+    want_sel, want_out = wl.oracle(ref)
+    sel, out = run_forward(msa, wl, "tensorcore")
+    assert_sel_equal(sel, want_sel)
+    assert_close(out, want_out)
+
+
 @pytest.mark.parametrize("kernels", KERNELS)
 def test_chunked_prefill_matches_whole(msa, ref, kernels):
     L = 2944
