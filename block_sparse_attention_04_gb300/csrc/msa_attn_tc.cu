@@ -171,7 +171,8 @@ template <int D>
 struct AttnCfg {
   static constexpr int kHalf = 128 * 128;              // one [128 rows][64] bf16 SW128 box
   static constexpr int kNHalf = D / 64;                // 64-dim halves of a row
-  static constexpr int kSmemQ = 2 * kHalf;             // Q tile, later P (128 x 128 tokens)
+  static constexpr int kQGroup = kNHalf * 1024;        // one 8-row group of the Q tile
+  static constexpr int kSmemQ = 16 * kQGroup;          // Q tile (128 rows)
   static constexpr int kSmemK = kNHalf * kHalf;
   static constexpr int kSmemV = kNHalf * kHalf;
   static constexpr int kSmem = kSmemQ + kSmemK + kSmemV + 256 + 1024;
@@ -255,12 +256,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   uint32_t it = 0;      // tiles processed by this CTA (phase of the per-tile barriers)
   uint32_t kv_it = 0;   // K/V loads issued by this CTA (phase of bar_k, bar_v)
   int prev_list = -1;
-  // Q boxes are 8 rows (heads) x 64 dims, one 128-byte-swizzle atom each:
-  // an entry takes rpe/8 boxes per 64-dim half, a tile at most 32 boxes, so
-  // lane j copies box j (entry-major, then half, then 8-row group).
-  const int bpe = a.rpe >> 3;                   // boxes per entry and half
-  const int box_e = lane / (bpe * C::kNHalf);   // this lane's entry
-  const int box_h = (lane / bpe) % C::kNHalf;   // its 64-dim half
+  // The Q tile is [8-row group][64-dim half][8 rows][64 dims]: one box of 8
+  // rows (heads) x all D dims fills one group, i.e. one 128-byte-swizzle
+  // atom per half.  An entry takes rpe/8 groups, a tile at most 16 boxes;
+  // lane j copies box j.
+  const int bpe = a.rpe >> 3;                   // groups (boxes) per entry
+  const int box_e = lane / bpe;                 // this lane's entry
   const int box_r = (lane % bpe) * 8;           // its first row within the entry
   // row of q (token * H + head) where this lane's box starts, for a tile;
   // loaded one tile ahead
@@ -312,9 +313,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       }
       __syncwarp();
       if (box_e < ne)
-        tma_load_2d(smem_u32(sQ + box_h * C::kHalf + (box_e * a.rpe + box_r) * 128), &tm_q, bar_q,
-                    box_h * 64, qrow);
-      if (tile + 1 < tile_hi) qrow = q_row(dnext);
+        tma_load_3d(smem_u32(sQ + ((box_e * a.rpe + box_r) >> 3) * C::kQGroup), &tm_q, bar_q, 0,
+                    qrow, 0);
       // V only for a new list.  The wait for the previous P.V happens only
       // then: a tile that reuses K/V needs nothing more from this warp, so its
       // own P.V may complete meanwhile, and a parity wait on a barrier two
@@ -328,6 +328,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         for (int h = 0; h < C::kNHalf; ++h)
           tma_load_3d(smem_u32(sV + h * C::kHalf), &tm_v, bar_v, h * 64, g, row);
       }
+      // the next tile's rows, while this warp waits for the next S anyway
+      if (tile + 1 < tile_hi) qrow = q_row(dnext);
     } else if (warp == 1) {
       // -------------------------------------------------- MMA (warp 1)
       // tcgen05.mma executes in issue order, so S of this tile cannot
@@ -343,9 +345,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * C::kHalf + (k & 3) * 32;
-            tc_mma_f16(tmem, smem_desc(q0 + off, 16, 1024, kSwizzle128B),
-                       smem_desc(k0 + off, 16, 1024, kSwizzle128B), idesc_s, k > 0);
+            const uint32_t kin = (k & 3) * 32;  // 16 dims within a 64-dim half
+            tc_mma_f16(tmem, smem_desc(q0 + (k >> 2) * 1024 + kin, 16, C::kQGroup, kSwizzle128B),
+                       smem_desc(k0 + (k >> 2) * C::kHalf + kin, 16, 1024, kSwizzle128B), idesc_s,
+                       k > 0);
           }
           tc_commit(bar_s);
           ok = mbar_wait(bar_p, ph, a.status) && mbar_wait(bar_v, kv_ph, a.status) &&
@@ -582,11 +585,12 @@ cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint
   const int rpe = hpg <= 8 ? 8 : 16;
   CUtensorMap tm_q, tm_k, tm_v;
   {
-    // q as [B*T*H rows][D]: one box = 8 rows (heads) x 64 dims
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)s.B * s.T * s.H};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, 8};
-    if (!encode_bf16_map(&tm_q, q, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    // q as (64 dims, B*T*H rows, D/64 halves): one box = 8 rows (heads) x all
+    // D dims, written half after half, i.e. one 8-row group of the Q tile
+    cuuint64_t dims[3] = {64, (cuuint64_t)s.B * s.T * s.H, (cuuint64_t)(D / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+    cuuint32_t box[3] = {64, 8, (cuuint32_t)(D / 64)};
+    if (!encode_bf16_map(&tm_q, q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   {
