@@ -389,6 +389,14 @@ def reference_arm(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the index
+# scan's kernels per msa_index_topk call, averaged over the calls of one step,
+# from a single-pass ncu capture of the same workload (the index scan traffic
+# summary under profiles/).  These are measurements of the kernels as they
+# were then: reset an entry to None whenever those kernels change.
+INDEX_TRAFFIC = {"prefill_1m": 1135872414, "decode_256k": 2152877056}
+
+
 def measure(name, args, world, rank):
     """Time workload `name`; returns the fields of its JSON line."""
     import torch
@@ -404,7 +412,7 @@ def measure(name, args, world, rank):
         roof = {"bound": "hbm",
                 "kernel": "index scan (msa_index_topk: index_stream + topk_merge)",
                 "achieved": kidx_b / (idx_ms / 1000.0) / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "traffic": None, "peak_kind": peak_kind,
+                "unit": "GB/s", "traffic": INDEX_TRAFFIC.get(name), "peak_kind": peak_kind,
                 "bytes_per_launch": kidx_b}
         roof["frac"] = roof["achieved"] / roof["peak"]
         whole = {"bytes_per_step": kidx_b + rest_b,
@@ -419,7 +427,8 @@ def measure(name, args, world, rank):
         roof = {"bound": "tensor",
                 "kernel": "index scan (msa_index_topk: index_tc + topk_merge)",
                 "achieved": fi / (idx_ms / 1000.0) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
-                "traffic": None, "peak_kind": peak_kind + (" sustained" if sustained else " burst"),
+                "traffic": INDEX_TRAFFIC.get(name),
+                "peak_kind": peak_kind + (" sustained" if sustained else " burst"),
                 "flops_per_step": fi, "launches_per_step": len(job.calls)}
         roof["frac"] = roof["achieved"] / roof["peak"]
         whole = {"flops_per_step": fi + fa, "index_flops": fi, "attn_flops": fa,
