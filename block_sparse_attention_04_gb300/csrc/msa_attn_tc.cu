@@ -419,8 +419,13 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int k = 2 * u;
-          float p0 = ex2(fmaf(__uint_as_float(v[k]), sl, -m));
-          float p1 = ex2(fmaf(__uint_as_float(v[k + 1]), sl, -m));
+          // 6 of 16 pairs on the FMA pipe, the rest on the MUFU unit
+          constexpr unsigned kPolyPairs = 0x4925u;  // u = 0, 2, 5, 8, 11, 14
+          const bool poly = (kPolyPairs >> u) & 1u;
+          const float x0 = fmaf(__uint_as_float(v[k]), sl, -m);
+          const float x1 = fmaf(__uint_as_float(v[k + 1]), sl, -m);
+          float p0 = poly ? exp2_poly(x0) : ex2(x0);
+          float p1 = poly ? exp2_poly(x1) : ex2(x1);
           if (masked) {
             p0 = c * 32 + k <= lim ? p0 : 0.f;
             p1 = c * 32 + k + 1 <= lim ? p1 : 0.f;

@@ -39,6 +39,23 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// 2^x for x <= 0 on the FMA pipe, to share exponentials with the MUFU unit:
+// x = j + f with j = round(x) and f in [-0.5, 0.5] (adding 1.5 * 2^23 leaves
+// round(x) in the low mantissa bits, exactly, for |x| < 2^22); 2^f is a
+// degree-3 polynomial fitted here for minimum relative error on [-0.5, 0.5]
+// (at most 7.5e-5, far below the bf16 rounding of attention weights); j goes
+// into the exponent bits (the constant's own bits vanish in the shift).
+// Arguments below -126 are clamped: the result is then about 1e-38.
+constexpr float kExp2C0 = 0.99992806f, kExp2C1 = 0.69326055f, kExp2C2 = 0.24261132f,
+                kExp2C3 = 0.05517394f;
+__device__ __forceinline__ float exp2_poly(float x) {
+  x = fmaxf(x, -126.f);
+  const float t = x + 12582912.f;
+  const float f = x - (t - 12582912.f);
+  const float p = fmaf(fmaf(fmaf(kExp2C3, f, kExp2C2), f, kExp2C1), f, kExp2C0);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
