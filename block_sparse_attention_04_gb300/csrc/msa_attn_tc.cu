@@ -6,17 +6,21 @@
 // A query-outer tile would hold one query's heads of one group (6 rows),
 // far below the 128 rows a tcgen05 MMA wants.  So the selections are inverted:
 // for every (sequence b, KV block kb, group g) the (query, slot) entries that
-// chose it.  One tile = one such block x up to R = 128/(H/G) entries, i.e.
-// R*(H/G) <= 128 query-head rows against the block's 128 tokens:
-//   TMA           K and V of block kb, KV head g (block-major cache: 128 rows of
-//                 D bf16 at stride G*D)
-//   warps 0-3     gather the Q rows of the tile's entries into swizzled smem
-//   warp 8        tcgen05.mma  S = Q K^T (TMEM)  and  O = P V (P read from
-//                 TMEM, V an MN-major smem operand)
-//   warps 4-7     row softmax of S (block-local max m, sum l; causal mask on the
-//                 local block), P as bf16 written over S in TMEM, (m, l) out
-//   warps 9-12    O as an unnormalised bf16 partial, overlapping the next
-//                 tile's softmax
+// chose it.  One tile = one such block x up to R entries, an entry's H/G heads
+// padded to rpe = 8 (or 16) rows, i.e. at most 128 query-head rows against
+// the block's 128 tokens.  One persistent CTA per SM runs two tile chains
+// (tile t on chain t & 1), so one chain's S = Q K^T runs while the other
+// chain's softmax works:
+//   warp 0        TMA of Q tiles (8-head x D boxes, one per 8-row group)
+//                 through a 3-deep ring: the Q copy is the longest latency
+//   warp 1        TMA of K and V blocks of KV head g (block-major cache: 128
+//                 rows of D bf16 at stride G*D) through 2-deep rings, one load
+//                 per list
+//   warp 2        tcgen05.mma, S(t) then P.V(t-1): S into TMEM, O = P V with P
+//                 read from TMEM and V an MN-major smem operand
+//   warps 3-10    row softmax, one warpgroup per chain (block-local max m, sum
+//                 l; causal mask on the local block), P as bf16 written over S
+//   warps 11-18   O as an unnormalised bf16 partial, one warpgroup per chain
 // Each (query, head, slot) partial (O, m, l) is combined by a log-sum-exp
 // merge into the bf16 output.
 #include <climits>
@@ -28,7 +32,9 @@
 namespace msa {
 namespace {
 
-constexpr int kAttnThreads = 320;  // 10 warps
+// warps: Q TMA, K/V TMA, MMA, 2 softmax warpgroups, 2 O-epilogue warpgroups
+constexpr int kQWarp = 0, kKVWarp = 1, kMmaWarp = 2, kSoftWarp0 = 3, kEpiWarp0 = 11;
+constexpr int kAttnThreads = 32 * 19;
 constexpr int kPassRows = 8192;    // (sequence, query) rows per pass
 
 struct AttnPass {
@@ -167,16 +173,19 @@ __global__ void csr_fill_kernel(AttnPass a) {
 }
 
 // ---- the attention tile kernel ---------------------------------------------
+constexpr int kQStages = 3;   // Q tiles in flight (the Q copy is the longest latency)
+constexpr int kKVStages = 2;  // K and V blocks in flight
+
 template <int D>
 struct AttnCfg {
   static constexpr int kHalf = 128 * 128;              // one [128 rows][64] bf16 SW128 box
   static constexpr int kNHalf = D / 64;                // 64-dim halves of a row
   static constexpr int kQGroup = kNHalf * 1024;        // one 8-row group of the Q tile
   static constexpr int kSmemQ = 16 * kQGroup;          // Q tile (128 rows)
-  static constexpr int kSmemK = kNHalf * kHalf;
-  static constexpr int kSmemV = kNHalf * kHalf;
-  static constexpr int kSmem = kSmemQ + kSmemK + kSmemV + 256 + 1024;
-  static constexpr uint32_t kTmemCols = 256;            // S [0,128) and O [128, 128+D)
+  static constexpr int kSmemK = kNHalf * kHalf;        // one K (or V) block of one KV head
+  static constexpr int kSmem = kQStages * kSmemQ + 2 * kKVStages * kSmemK + 256 + 1024;
+  // two chains: S/P at [0,128) and [128,256), O at [256,384) and [384,512)
+  static constexpr uint32_t kTmemCols = 512;
 };
 
 // Maximum / minimum of 32 fp32 values held as raw bits (3-input trees).
@@ -202,36 +211,48 @@ __device__ __forceinline__ float tree_min32(const uint32_t (&v)[32]) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 2)
+__global__ void __launch_bounds__(kAttnThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const AttnPass a) {
   using C = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t* sQ = smem;  // Q of the tile (P lives in TMEM)
-  uint8_t* sK = smem + C::kSmemQ;
-  uint8_t* sV = sK + C::kSmemK;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + C::kSmemV);
-  uint64_t* bar_k = bars + 0;
-  uint64_t* bar_q = bars + 1;
-  uint64_t* bar_s = bars + 2;
-  uint64_t* bar_p = bars + 3;
-  uint64_t* bar_o = bars + 4;
-  uint64_t* bar_done = bars + 5;
-  uint64_t* bar_fin = bars + 6;
-  uint64_t* bar_v = bars + 7;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  uint8_t* sQ = smem;                                  // [kQStages] Q tiles
+  uint8_t* sK = sQ + kQStages * C::kSmemQ;             // [kKVStages] K blocks
+  uint8_t* sV = sK + kKVStages * C::kSmemK;            // [kKVStages] V blocks
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kKVStages * C::kSmemK);
+  uint64_t* q_full = bars;                        // kQStages
+  uint64_t* q_empty = q_full + kQStages;          // kQStages
+  uint64_t* k_full = q_empty + kQStages;          // kKVStages
+  uint64_t* k_empty = k_full + kKVStages;
+  uint64_t* v_full = k_empty + kKVStages;
+  uint64_t* v_empty = v_full + kKVStages;
+  uint64_t* s_full = v_empty + kKVStages;         // per chain: S of its tile is in TMEM
+  uint64_t* p_full = s_full + 2;                  // per chain: P written over S
+  uint64_t* o_full = p_full + 2;                  // per chain: O of its tile is in TMEM
+  uint64_t* o_empty = o_full + 2;                 // per chain: O read out
+  uint64_t* bar_fin = o_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_fin + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(bar_k, 1);
-    mbar_init(bar_v, 1);
-    mbar_init(bar_q, 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_p, 128);
-    mbar_init(bar_o, 1);
-    mbar_init(bar_done, 128);
+    for (int i = 0; i < kQStages; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    for (int i = 0; i < kKVStages; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int c = 0; c < 2; ++c) {
+      mbar_init(&s_full[c], 1);
+      mbar_init(&p_full[c], 128);
+      mbar_init(&o_full[c], 1);
+      mbar_init(&o_empty[c], 128);
+    }
     mbar_init(bar_fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -239,7 +260,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -247,157 +268,198 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 
   const int H = a.s.H, hpg = H / a.s.G;
   const int rshift = a.rpe == 8 ? 3 : 4;  // tile row -> entry
-  // a contiguous range of tiles per CTA: consecutive tiles of one list reuse
-  // the K/V block already in shared memory
+  // a contiguous range of tiles per CTA: consecutive tiles of one list share
+  // the K/V block in shared memory
   const int ntiles = a.tile_off[a.nlists];
   const int per = (ntiles + gridDim.x - 1) / gridDim.x;
   const int tile_lo = blockIdx.x * per;
-  const int tile_hi = min(ntiles, tile_lo + per);
-  uint32_t it = 0;      // tiles processed by this CTA (phase of the per-tile barriers)
-  uint32_t kv_it = 0;   // K/V loads issued by this CTA (phase of bar_k, bar_v)
-  int prev_list = -1;
-  // The Q tile is [8-row group][64-dim half][8 rows][64 dims]: one box of 8
-  // rows (heads) x all D dims fills one group, i.e. one 128-byte-swizzle
-  // atom per half.  An entry takes rpe/8 groups, a tile at most 16 boxes;
-  // lane j copies box j.
-  const int bpe = a.rpe >> 3;                   // groups (boxes) per entry
-  const int box_e = lane / bpe;                 // this lane's entry
-  const int box_r = (lane % bpe) * 8;           // its first row within the entry
-  // row of q (token * H + head) where this lane's box starts, for a tile;
-  // loaded one tile ahead
-  auto q_row = [&](const int4& dd) -> int {
-    if (box_e >= dd.z) return 0;
-    const int il = a.entries[dd.y + box_e] >> 4;
-    return (int)((((int64_t)(dd.w >> 18) * a.s.T + a.t0 + il) * H) + ((dd.w >> 15) & 7) * hpg +
-                 box_r);
-  };
-  int qrow = 0;
-  // the next tile's descriptor is loaded one iteration ahead
-  int4 dnext = tile_lo < tile_hi ? a.tile_desc[tile_lo] : make_int4(0, 0, 0, 0);
-  for (int tile = tile_lo; tile < tile_hi; ++tile, ++it) {
-    if (*abort_flag) break;
-    const uint32_t ph = it & 1;
-    const int4 d = dnext;
-    if (tile + 1 < tile_hi) dnext = a.tile_desc[tile + 1];
-    const int L = d.x;
-    const bool reuse_kv = (L == prev_list);
-    prev_list = L;
-    const uint32_t kv_ph = reuse_kv ? ((kv_it - 1) & 1) : (kv_it & 1);
-    if (!reuse_kv) ++kv_it;
-    const int kb = d.w & 0x7FFF;
-    const int g = (d.w >> 15) & 7;
-    const int b = d.w >> 18;
-    const int ne = d.z;
-    const int32_t* ent = a.entries + d.y;
+  const int n = max(0, min(ntiles, tile_lo + per) - tile_lo);  // tiles of this CTA
+  const int4* desc = a.tile_desc + tile_lo;
 
-    if (warp == 0) {
-      // ------------------------------------------------------ TMA (warp 0)
-      // Q and K of this tile once S of the previous tile is done (P lives in
-      // TMEM, so the Q buffer is free then); V once its P.V is done.  Entry e
-      // fills tile rows [e*rpe, e*rpe + rpe): its hpg heads, then heads of the
-      // next group or token (or zero fill past the end), which land in rows
-      // the softmax and epilogue skip.
-      if (tile == tile_lo) qrow = q_row(d);
-      if (it > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_s, ph ^ 1, a.status))) { *abort_flag = 1; break; }
+  if (warp == kQWarp) {
+    // ---------------------------------------------------- Q TMA (warp 0)
+    // Q tiles through a kQStages ring: the Q of tile t is loaded once S of
+    // tile t - kQStages is done, i.e. well before S of t is due.  Entry e
+    // fills tile rows [e*rpe, e*rpe + rpe) (its hpg heads, then heads of the
+    // next group or token, or zero fill past the end: rows the softmax and
+    // epilogue skip), one box of 8 rows x D dims per lane.  L2 policy: Q rows
+    // are read again for each block their query selected (evict last).
+    const uint64_t pol_q = l2_policy_evict_last();
+    const int bpe = a.rpe >> 3;                   // boxes per entry
+    const int box_e = lane / bpe;                 // this lane's entry
+    const int box_r = (lane % bpe) * 8;           // its first row within the entry
+    for (int t = 0; t < n; ++t) {
+      const int4 d = desc[t];
+      const int ne = d.z;
+      int qrow = 0;
+      if (box_e < ne) {
+        const int il = a.entries[d.y + box_e] >> 4;
+        qrow = (int)(((int64_t)(d.w >> 18) * a.s.T + a.t0 + il) * H + ((d.w >> 15) & 7) * hpg +
+                     box_r);
       }
-      const int row = (int)(((int64_t)b * a.s.max_blocks + kb) * kBlock);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar_q, (uint32_t)(ne * a.rpe * D * 2));
-        if (!reuse_kv) {
-          mbar_arrive_expect_tx(bar_k, C::kNHalf * C::kHalf);
-#pragma unroll
-          for (int h = 0; h < C::kNHalf; ++h)
-            tma_load_3d(smem_u32(sK + h * C::kHalf), &tm_k, bar_k, h * 64, g, row);
-        }
+      const int qs = t % kQStages;
+      const uint32_t u = (uint32_t)(t / kQStages);
+      if (!__all_sync(0xffffffffu, mbar_wait(&q_empty[qs], (u & 1) ^ 1, a.status))) {
+        *abort_flag = 1;
+        break;
       }
+      if (lane == 0) mbar_arrive_expect_tx(&q_full[qs], (uint32_t)(ne * a.rpe * D * 2));
       __syncwarp();
       if (box_e < ne)
-        tma_load_3d(smem_u32(sQ + ((box_e * a.rpe + box_r) >> 3) * C::kQGroup), &tm_q, bar_q, 0,
-                    qrow, 0);
-      // V only for a new list.  The wait for the previous P.V happens only
-      // then: a tile that reuses K/V needs nothing more from this warp, so its
-      // own P.V may complete meanwhile, and a parity wait on a barrier two
-      // phases ahead would never return.
-      if (it > 0 && !reuse_kv) {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_o, ph ^ 1, a.status))) { *abort_flag = 1; break; }
-      }
-      if (lane == 0 && !reuse_kv) {
-        mbar_arrive_expect_tx(bar_v, C::kNHalf * C::kHalf);
+        tma_load_3d_hint(smem_u32(sQ + qs * C::kSmemQ + ((box_e * a.rpe + box_r) >> 3) * C::kQGroup),
+                         &tm_q, &q_full[qs], 0, qrow, 0, pol_q);
+    }
+  } else if (warp == kKVWarp) {
+    // -------------------------------------------------- K/V TMA (warp 1)
+    // One K and one V block per list change, through a kKVStages ring; a
+    // buffer is refilled once the last tile of its previous list is through
+    // S (K) or P.V (V).  L2 policy: evict first (used once, from smem).
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_policy_evict_first();
+      int kv = -1, prev = -1;
+      for (int t = 0; t < n && !*abort_flag; ++t) {
+        const int4 d = desc[t];
+        if (d.x == prev) continue;
+        prev = d.x;
+        ++kv;
+        const int ks = kv % kKVStages;
+        const uint32_t w = (uint32_t)(kv / kKVStages);
+        const int kb = d.w & 0x7FFF, g = (d.w >> 15) & 7, b = d.w >> 18;
+        const int row = (int)(((int64_t)b * a.s.max_blocks + kb) * kBlock);
+        if (!mbar_wait(&k_empty[ks], (w & 1) ^ 1, a.status)) { *abort_flag = 1; break; }
+        mbar_arrive_expect_tx(&k_full[ks], C::kSmemK);
 #pragma unroll
         for (int h = 0; h < C::kNHalf; ++h)
-          tma_load_3d(smem_u32(sV + h * C::kHalf), &tm_v, bar_v, h * 64, g, row);
+          tma_load_3d_hint(smem_u32(sK + ks * C::kSmemK + h * C::kHalf), &tm_k, &k_full[ks], h * 64, g,
+                           row, pol_kv);
+        if (!mbar_wait(&v_empty[ks], (w & 1) ^ 1, a.status)) { *abort_flag = 1; break; }
+        mbar_arrive_expect_tx(&v_full[ks], C::kSmemK);
+#pragma unroll
+        for (int h = 0; h < C::kNHalf; ++h)
+          tma_load_3d_hint(smem_u32(sV + ks * C::kSmemK + h * C::kHalf), &tm_v, &v_full[ks], h * 64, g,
+                           row, pol_kv);
       }
-      // the next tile's rows, while this warp waits for the next S anyway
-      if (tile + 1 < tile_hi) qrow = q_row(dnext);
-    } else if (warp == 1) {
-      // -------------------------------------------------- MMA (warp 1)
-      // tcgen05.mma executes in issue order, so S of this tile cannot
-      // overwrite the P that the previous P.V still reads; P.V of this tile
-      // waits for the previous O to have been read out.
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------ MMA (warp 2)
+    // Order S(0), S(1), P.V(0), S(2), P.V(1), ...: the S of one chain runs
+    // while the other chain's softmax works.  Tile t uses chain c = t & 1:
+    // S and P in TMEM columns [128c, 128c + 128), O in [256 + 128c, ...).
+    // tcgen05.mma executes in issue order, so S(t + 2) cannot overwrite the P
+    // that P.V(t), issued before it, still reads.
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
+      int kv = -1, prev = -1;
+      int pv_ks = 0;
+      uint32_t pv_w = 0;
+      bool pv_last = false, pv_first = false;
       bool ok = true;
-      if (lane == 0) {
-        constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
-        constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
-        ok = mbar_wait(bar_q, ph, a.status) && mbar_wait(bar_k, kv_ph, a.status);
-        if (ok) {
+      // the lists of tiles t and t + 1, loaded two tiles ahead (a load takes
+      // about as long as issuing a tile's MMAs)
+      int l0 = n > 0 ? desc[0].x : -1, l1 = n > 1 ? desc[1].x : -1;
+      for (int t = 0; t <= n && ok; ++t) {
+        int ks = 0;
+        uint32_t w = 0;
+        bool last = false, first = false;
+        const int lt = l0, ln = l1;
+        l0 = l1;
+        l1 = t + 2 < n ? desc[t + 2].x : -1;
+        if (t < n) {
+          // ---- S(t)
+          first = lt != prev;  // K and V are waited for once per list
+          if (first) { prev = lt; ++kv; }
+          ks = kv % kKVStages;
+          w = (uint32_t)(kv / kKVStages);
+          last = (t + 1 == n) || ln != lt;
+          const int c = t & 1, qs = t % kQStages;
+          ok = mbar_wait(&q_full[qs], (uint32_t)(t / kQStages) & 1, a.status) &&
+               (!first || mbar_wait(&k_full[ks], w & 1, a.status));
+          if (!ok) break;
           tc_fence_after();
-          const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
+          const uint32_t q0 = smem_u32(sQ + qs * C::kSmemQ), k0 = smem_u32(sK + ks * C::kSmemK);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t kin = (k & 3) * 32;  // 16 dims within a 64-dim half
-            tc_mma_f16(tmem, smem_desc(q0 + (k >> 2) * 1024 + kin, 16, C::kQGroup, kSwizzle128B),
+            tc_mma_f16(tmem + c * 128,
+                       smem_desc(q0 + (k >> 2) * 1024 + kin, 16, C::kQGroup, kSwizzle128B),
                        smem_desc(k0 + (k >> 2) * C::kHalf + kin, 16, 1024, kSwizzle128B), idesc_s,
                        k > 0);
           }
-          tc_commit(bar_s);
-          ok = mbar_wait(bar_p, ph, a.status) && mbar_wait(bar_v, kv_ph, a.status) &&
-               (it == 0 || mbar_wait(bar_done, ph ^ 1, a.status));
-          if (ok) {
-            tc_fence_after();
-            // P (bf16, two per column) is in TMEM columns [0, 64): 8 per 16 tokens
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              tc_mma_f16_ts(tmem + 128, tmem + k * 8,
-                            smem_desc(v0 + k * 2048, C::kHalf, 1024, kSwizzle128B), idesc_o, k > 0);
-            tc_commit(bar_o);
-          }
+          tc_commit(&q_empty[qs]);
+          tc_commit(&s_full[c]);
+          if (last) tc_commit(&k_empty[ks]);
         }
+        if (t >= 1) {
+          // ---- P.V(t - 1)
+          const int tp = t - 1, c = tp & 1;
+          const uint32_t j = (uint32_t)(tp >> 1);
+          ok = mbar_wait(&p_full[c], j & 1, a.status) &&
+               (!pv_first || mbar_wait(&v_full[pv_ks], pv_w & 1, a.status)) &&
+               (j == 0 || mbar_wait(&o_empty[c], (j - 1) & 1, a.status));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t v0 = smem_u32(sV + pv_ks * C::kSmemK);
+          // P (bf16, two per column) is in TMEM columns [128c, 128c + 64)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            tc_mma_f16_ts(tmem + 256 + c * 128, tmem + c * 128 + k * 8,
+                          smem_desc(v0 + k * 2048, C::kHalf, 1024, kSwizzle128B), idesc_o, k > 0);
+          tc_commit(&o_full[c]);
+          if (pv_last) tc_commit(&v_empty[pv_ks]);
+        }
+        pv_ks = ks;
+        pv_w = w;
+        pv_last = last;
+        pv_first = first;
       }
-      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { *abort_flag = 1; break; }
-    } else if (warp < 6) {
-      // -------------------------------------------------- softmax (warps 2-5)
-      const int quad = warp & 3;
-      const int r = quad * 32 + lane;  // tile row = TMEM lane
+      if (!ok) *abort_flag = 1;
+      // all MMAs done before TMEM is released
+      tc_commit(bar_fin);
+      mbar_wait(bar_fin, 0, nullptr);
+    }
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------ softmax (2 warpgroups, one per chain)
+    const int c = (warp - kSoftWarp0) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // tile row = TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + c * 128;
+    const float sl = a.s.scale * kLog2e;
+    for (int t = c; t < n; t += 2) {
+      if (*abort_flag) break;
+      const int4 d = desc[t];
+      const int kb = d.w & 0x7FFF, g = (d.w >> 15) & 7, b = d.w >> 18;
       const int e = r >> rshift, hh = r & (a.rpe - 1);
-      const bool valid = e < ne && hh < hpg;
+      const bool valid = e < d.z && hh < hpg;
       int il = 0, slot = 0;
       if (valid) {
-        il = ent[e] >> 4;
-        slot = ent[e] & 15;
+        const int en = a.entries[d.y + e];
+        il = en >> 4;
+        slot = en & 15;
       }
-      const int64_t t = (int64_t)a.pos.q_start[b] + a.t0 + il;
-      // tokens kb*128 + c with c > lim are masked (only in the local block)
-      const int lim = (int)(t - (int64_t)kb * kBlock);
+      const int64_t tq = (int64_t)a.pos.q_start[b] + a.t0 + il;
+      // tokens kb*128 + col with col > lim are masked (only in the local block)
+      const int lim = (int)(tq - (int64_t)kb * kBlock);
       const bool masked = __any_sync(0xffffffffu, valid && lim < kBlock - 1);
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_s, ph, a.status))) { *abort_flag = 1; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[c], (uint32_t)(t >> 1) & 1, a.status))) {
+        *abort_flag = 1;
+        break;
+      }
       tc_fence_after();
-      const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-      const float sl = a.s.scale * kLog2e;
       uint32_t v[32];
       // pass 1: row maximum of the scaled scores: the maximum of the raw
       // scores, or their minimum when the scale is negative
       const bool neg = sl < 0.f;
       float mx = neg ? INFINITY : -INFINITY;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(lane_base + c * 32, v);
+      for (int cc = 0; cc < 4; ++cc) {
+        tmem_ld32(lane_base + cc * 32, v);
         tmem_ld_wait();
         if (masked) {
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
             const float x = __uint_as_float(v[k]);
-            const bool in = c * 32 + k <= lim;
+            const bool in = cc * 32 + k <= lim;
             mx = neg ? fminf(mx, in ? x : INFINITY) : fmaxf(mx, in ? x : -INFINITY);
           }
         } else if (!neg) {
@@ -408,14 +470,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
       }
       const float m = mx * sl;
       // pass 2: P = 2^(s*scale*log2e - m) as bf16, two per column, written
-      // over S in TMEM (chunk c of S is read before columns [16c, 16c+16) are
-      // written, and those columns belong to chunks already read); row sum
+      // over S in TMEM (chunk cc of S is read before columns [16cc, 16cc+16)
+      // are written, and those columns belong to chunks already read); row sum
       float l0 = 0.f, l1 = 0.f;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(lane_base + c * 32, v);
+      for (int cc = 0; cc < 4; ++cc) {
+        tmem_ld32(lane_base + cc * 32, v);
         tmem_ld_wait();
-        uint32_t w[16];
+        uint32_t wv[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int k = 2 * u;
@@ -427,43 +489,52 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
           float p0 = poly ? exp2_poly(x0) : ex2(x0);
           float p1 = poly ? exp2_poly(x1) : ex2(x1);
           if (masked) {
-            p0 = c * 32 + k <= lim ? p0 : 0.f;
-            p1 = c * 32 + k + 1 <= lim ? p1 : 0.f;
+            p0 = cc * 32 + k <= lim ? p0 : 0.f;
+            p1 = cc * 32 + k + 1 <= lim ? p1 : 0.f;
           }
           l0 += p0;
           l1 += p1;
-          w[u] = pack_bf16(p0, p1);
+          wv[u] = pack_bf16(p0, p1);
         }
-        tmem_st16(lane_base + c * 16, w);
+        tmem_st16(lane_base + cc * 16, wv);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_p);
+      mbar_arrive(&p_full[c]);
       if (valid) {
         const size_t prow = (((size_t)b * a.Tp + il) * H + (size_t)g * hpg + hh) * kTopk + slot;
         __stcs(a.part_ml + prow, make_float2(m, l0 + l1));
       }
-    } else {
-      // -------------------------------------------- O epilogue (warps 6-9)
-      // O = P.V (unnormalised) as a bf16 partial; the merge divides by the
-      // combined sum.  Runs while the softmax warps work on the next tile.
-      const int quad = warp & 3;
-      const int r = quad * 32 + lane;
+    }
+  } else {
+    // ------------------------------------ O epilogue (2 warpgroups, one per chain)
+    // O = P.V (unnormalised) as a bf16 partial; the merge divides by the
+    // combined sum.
+    const int c = (warp - kEpiWarp0) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + 256 + c * 128;
+    for (int t = c; t < n; t += 2) {
+      if (*abort_flag) break;
+      const int4 d = desc[t];
+      const int g = (d.w >> 15) & 7, b = d.w >> 18;
       const int e = r >> rshift, hh = r & (a.rpe - 1);
-      const bool valid = e < ne && hh < hpg;
+      const bool valid = e < d.z && hh < hpg;
       size_t prow = 0;
       if (valid) {
-        const int en = ent[e];
+        const int en = a.entries[d.y + e];
         prow = (((size_t)b * a.Tp + (en >> 4)) * H + (size_t)g * hpg + hh) * kTopk + (en & 15);
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_o, ph, a.status))) { *abort_flag = 1; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(&o_full[c], (uint32_t)(t >> 1) & 1, a.status))) {
+        *abort_flag = 1;
+        break;
+      }
       tc_fence_after();
-      const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + 128;
       uint16_t* dst = a.part_o + prow * D;
       uint32_t v[32];
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(lane_base + c * 32, v);
+      for (int cc = 0; cc < D / 32; ++cc) {
+        tmem_ld32(lane_base + cc * 32, v);
         tmem_ld_wait();
         if (valid) {
 #pragma unroll
@@ -473,25 +544,19 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
             pk.y = pack_bf16(__uint_as_float(v[e8 * 8 + 2]), __uint_as_float(v[e8 * 8 + 3]));
             pk.z = pack_bf16(__uint_as_float(v[e8 * 8 + 4]), __uint_as_float(v[e8 * 8 + 5]));
             pk.w = pack_bf16(__uint_as_float(v[e8 * 8 + 6]), __uint_as_float(v[e8 * 8 + 7]));
-            // streaming store: the partial is read once, by the merge, and
-            // should not push Q and K/V out of L2
-            __stcs(reinterpret_cast<uint4*>(dst + c * 32 + e8 * 8), pk);
+            // streaming store: the partial is read once, by the merge
+            __stcs(reinterpret_cast<uint4*>(dst + cc * 32 + e8 * 8), pk);
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(bar_done);
+      mbar_arrive(&o_empty[c]);
     }
   }
 
-  // all MMAs done before TMEM is released
-  if (warp == 1 && lane == 0) {
-    tc_commit(bar_fin);
-    mbar_wait(bar_fin, 0, nullptr);
-  }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -610,11 +675,9 @@ cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  // Two CTAs per SM fit (2 x 256 TMEM columns, 2 x ~100 KiB smem, 84
-  // registers); ask for the shared-memory carveout that allows it.  CTAs do
-  // not depend on one another, so fewer resident CTAs only serialise.
+  // one CTA per SM: all 512 TMEM columns and ~225 KiB of shared memory
   cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  const int grid = 2 * sm_count();
+  const int grid = sm_count();
   const int tp_max = pass_len(s);
   for (int t0 = 0; t0 < s.T; t0 += tp_max) {
     AttnPass a;
