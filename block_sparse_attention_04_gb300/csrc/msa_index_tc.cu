@@ -15,7 +15,7 @@
 //               into one of two TMEM accumulator stages;
 //   warps 2-17  epilogue, four warpgroups: two read each accumulator stage
 //               (one key block each), stages alternate between the two
-//               pairs; tcgen05.ld of the row's 128 fp32 scores in 32-column
+//               pairs; tcgen05.ld of the row's 128 fp32 scores in 16-column
 //               chunks, block maximum (3-input max), insertion into a
 //               register-resident top-15 (score desc, block id asc); the four
 //               lists merge through shared memory at the end of the item.
@@ -321,39 +321,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!__all_sync(0xffffffffu, mbar_wait(&tm_full[my_ts], tphase, a.status))) { ok = false; break; }
         tphase ^= 1;
         tc_fence_after();
-        uint32_t v[32];
-        float m;
-        tmem_ld32(lane_base, v);
-        tmem_ld_wait();
-        m = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+        // eight 16-column loads, each waited before the next is issued: small
+        // loads leave the concurrently accumulating MMA more of tensor memory
+        // than larger or overlapped ones (measured)
+        uint32_t v[16];
+        float m = -INFINITY;
 #pragma unroll
-        for (int c = 1; c < 4; ++c) {
-          float mc[11];
-#pragma unroll
-          for (int k = 0; k < 10; ++k)
-            mc[k] = fmax3(__uint_as_float(v[3 * k + 2]), __uint_as_float(v[3 * k + 3]),
-                          __uint_as_float(v[3 * k + 4]));
-          mc[10] = __uint_as_float(v[31]);
-          tmem_ld32(lane_base + c * 32, v);
-          const float x = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]),
-                                fmax3(mc[6], mc[7], mc[8]));
-          m = fmax3(m, x, fmaxf(mc[9], mc[10]));
+        for (int c = 0; c < 8; ++c) {
+          tmem_ld16(lane_base + c * 16, v);
           tmem_ld_wait();
-          m = fmax3(m, __uint_as_float(v[0]), __uint_as_float(v[1]));
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tm_empty[my_ts]);
-        {
-          float mc[11];
-#pragma unroll
-          for (int k = 0; k < 10; ++k)
-            mc[k] = fmax3(__uint_as_float(v[3 * k + 2]), __uint_as_float(v[3 * k + 3]),
-                          __uint_as_float(v[3 * k + 4]));
-          mc[10] = __uint_as_float(v[31]);
-          const float x = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]),
-                                fmax3(mc[6], mc[7], mc[8]));
-          m = fmax3(m, x, fmaxf(mc[9], mc[10]));
+          if (c == 7) {  // the stage's scores are all in registers
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tm_empty[my_ts]);
+          }
+          const float x0 = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+          const float x1 = fmax3(__uint_as_float(v[3]), __uint_as_float(v[4]), __uint_as_float(v[5]));
+          const float x2 = fmax3(__uint_as_float(v[6]), __uint_as_float(v[7]), __uint_as_float(v[8]));
+          const float x3 = fmax3(__uint_as_float(v[9]), __uint_as_float(v[10]), __uint_as_float(v[11]));
+          const float x4 =
+              fmax3(__uint_as_float(v[12]), __uint_as_float(v[13]), __uint_as_float(v[14]));
+          m = fmax3(m, fmax3(x0, x1, x2), fmax3(x3, x4, __uint_as_float(v[15])));
         }
         const int blk = k0 + 2 * q + half;
         if (valid && blk < k1 && blk < lb && m > sc[kCand - 1]) list_insert_newest(sc, id, m, blk);
