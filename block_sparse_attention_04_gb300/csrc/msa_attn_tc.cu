@@ -188,26 +188,22 @@ struct AttnCfg {
   static constexpr uint32_t kTmemCols = 512;
 };
 
-// Maximum / minimum of 32 fp32 values held as raw bits (3-input trees).
-__device__ __forceinline__ float tree_max32(const uint32_t (&v)[32]) {
-  float t[11];
+// Maximum / minimum of 16 fp32 values held as raw bits (3-input trees).
+__device__ __forceinline__ float tree_max16(const uint32_t (&v)[16]) {
+  float t[5];
 #pragma unroll
-  for (int k = 0; k < 10; ++k)
+  for (int k = 0; k < 5; ++k)
     t[k] = fmax3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]),
                  __uint_as_float(v[3 * k + 2]));
-  t[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
-  return fmax3(fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], t[8])),
-               t[9], t[10]);
+  return fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], __uint_as_float(v[15])), -INFINITY);
 }
-__device__ __forceinline__ float tree_min32(const uint32_t (&v)[32]) {
-  float t[11];
+__device__ __forceinline__ float tree_min16(const uint32_t (&v)[16]) {
+  float t[5];
 #pragma unroll
-  for (int k = 0; k < 10; ++k)
+  for (int k = 0; k < 5; ++k)
     t[k] = fmin3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]),
                  __uint_as_float(v[3 * k + 2]));
-  t[10] = fminf(__uint_as_float(v[30]), __uint_as_float(v[31]));
-  return fmin3(fmin3(fmin3(t[0], t[1], t[2]), fmin3(t[3], t[4], t[5]), fmin3(t[6], t[7], t[8])),
-               t[9], t[10]);
+  return fmin3(fmin3(t[0], t[1], t[2]), fmin3(t[3], t[4], __uint_as_float(v[15])), INFINITY);
 }
 
 template <int D>
@@ -446,55 +442,62 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t v[32];
+      // TMEM is read in 16-column loads, each waited before the next: small
+      // loads leave the MMAs of the other chain more of tensor memory than
+      // larger ones (measured).
       // pass 1: row maximum of the scaled scores: the maximum of the raw
       // scores, or their minimum when the scale is negative
       const bool neg = sl < 0.f;
       float mx = neg ? INFINITY : -INFINITY;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        tmem_ld32(lane_base + cc * 32, v);
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t h[16];
+        tmem_ld16(lane_base + cc * 16, h);
         tmem_ld_wait();
         if (masked) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float x = __uint_as_float(v[k]);
-            const bool in = cc * 32 + k <= lim;
+          for (int k = 0; k < 16; ++k) {
+            const float x = __uint_as_float(h[k]);
+            const bool in = cc * 16 + k <= lim;
             mx = neg ? fminf(mx, in ? x : INFINITY) : fmaxf(mx, in ? x : -INFINITY);
           }
-        } else if (!neg) {
-          mx = fmax3(mx, tree_max32(v), -INFINITY);
         } else {
-          mx = fmin3(mx, tree_min32(v), INFINITY);
+          mx = neg ? fminf(mx, tree_min16(h)) : fmaxf(mx, tree_max16(h));
         }
       }
       const float m = mx * sl;
       // pass 2: P = 2^(s*scale*log2e - m) as bf16, two per column, written
-      // over S in TMEM (chunk cc of S is read before columns [16cc, 16cc+16)
-      // are written, and those columns belong to chunks already read); row sum
+      // over S in TMEM: the 32 scores of columns [32cc, 32cc+32) are read (two
+      // loads) before columns [16cc, 16cc+16) are written, and those belong to
+      // chunks already read; row sum
       float l0 = 0.f, l1 = 0.f;
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
-        tmem_ld32(lane_base + cc * 32, v);
-        tmem_ld_wait();
         uint32_t wv[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int k = 2 * u;
-          // 6 of 16 pairs on the FMA pipe, the rest on the MUFU unit
-          constexpr unsigned kPolyPairs = 0x4925u;  // u = 0, 2, 5, 8, 11, 14
-          const bool poly = (kPolyPairs >> u) & 1u;
-          const float x0 = fmaf(__uint_as_float(v[k]), sl, -m);
-          const float x1 = fmaf(__uint_as_float(v[k + 1]), sl, -m);
-          float p0 = poly ? exp2_poly(x0) : ex2(x0);
-          float p1 = poly ? exp2_poly(x1) : ex2(x1);
-          if (masked) {
-            p0 = cc * 32 + k <= lim ? p0 : 0.f;
-            p1 = cc * 32 + k + 1 <= lim ? p1 : 0.f;
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t h[16];
+          tmem_ld16(lane_base + cc * 32 + hf * 16, h);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int k = 2 * u;
+            const int uu = hf * 8 + u;
+            // 6 of 16 pairs on the FMA pipe, the rest on the MUFU unit
+            constexpr unsigned kPolyPairs = 0x4925u;  // uu = 0, 2, 5, 8, 11, 14
+            const bool poly = (kPolyPairs >> uu) & 1u;
+            const float x0 = fmaf(__uint_as_float(h[k]), sl, -m);
+            const float x1 = fmaf(__uint_as_float(h[k + 1]), sl, -m);
+            float p0 = poly ? exp2_poly(x0) : ex2(x0);
+            float p1 = poly ? exp2_poly(x1) : ex2(x1);
+            if (masked) {
+              p0 = cc * 32 + hf * 16 + k <= lim ? p0 : 0.f;
+              p1 = cc * 32 + hf * 16 + k + 1 <= lim ? p1 : 0.f;
+            }
+            l0 += p0;
+            l1 += p1;
+            wv[uu] = pack_bf16(p0, p1);
           }
-          l0 += p0;
-          l1 += p1;
-          wv[u] = pack_bf16(p0, p1);
         }
         tmem_st16(lane_base + cc * 16, wv);
       }
@@ -531,21 +534,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       tc_fence_after();
       uint16_t* dst = a.part_o + prow * D;
-      uint32_t v[32];
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        tmem_ld32(lane_base + cc * 32, v);
+      for (int cc = 0; cc < D / 16; ++cc) {
+        uint32_t h[16];
+        tmem_ld16(lane_base + cc * 16, h);
         tmem_ld_wait();
         if (valid) {
 #pragma unroll
-          for (int e8 = 0; e8 < 4; ++e8) {
+          for (int e8 = 0; e8 < 2; ++e8) {
             uint4 pk;
-            pk.x = pack_bf16(__uint_as_float(v[e8 * 8 + 0]), __uint_as_float(v[e8 * 8 + 1]));
-            pk.y = pack_bf16(__uint_as_float(v[e8 * 8 + 2]), __uint_as_float(v[e8 * 8 + 3]));
-            pk.z = pack_bf16(__uint_as_float(v[e8 * 8 + 4]), __uint_as_float(v[e8 * 8 + 5]));
-            pk.w = pack_bf16(__uint_as_float(v[e8 * 8 + 6]), __uint_as_float(v[e8 * 8 + 7]));
-            // streaming store: the partial is read once, by the merge
-            __stcs(reinterpret_cast<uint4*>(dst + cc * 32 + e8 * 8), pk);
+            pk.x = pack_bf16(__uint_as_float(h[e8 * 8 + 0]), __uint_as_float(h[e8 * 8 + 1]));
+            pk.y = pack_bf16(__uint_as_float(h[e8 * 8 + 2]), __uint_as_float(h[e8 * 8 + 3]));
+            pk.z = pack_bf16(__uint_as_float(h[e8 * 8 + 4]), __uint_as_float(h[e8 * 8 + 5]));
+            pk.w = pack_bf16(__uint_as_float(h[e8 * 8 + 6]), __uint_as_float(h[e8 * 8 + 7]));
+            __stcs(reinterpret_cast<uint4*>(dst + cc * 16 + e8 * 8), pk);
           }
         }
       }
