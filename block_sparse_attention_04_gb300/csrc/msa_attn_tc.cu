@@ -284,6 +284,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int bpe = a.rpe >> 3;                   // boxes per entry
     const int box_e = lane / bpe;                 // this lane's entry
     const int box_r = (lane % bpe) * 8;           // its first row within the entry
+    int q_last[kQStages];                         // last tile loaded into each slot
+#pragma unroll
+    for (int i = 0; i < kQStages; ++i) q_last[i] = -1;
     for (int t = 0; t < n; ++t) {
       const int4 d = desc[t];
       const int ne = d.z;
@@ -304,6 +307,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (box_e < ne)
         tma_load_3d_hint(smem_u32(sQ + qs * C::kSmemQ + ((box_e * a.rpe + box_r) >> 3) * C::kQGroup),
                          &tm_q, &q_full[qs], 0, qrow, 0, pol_q);
+      q_last[qs] = t;
+    }
+    // no copy may still be landing in shared memory when the CTA exits (after
+    // a timeout elsewhere the tiles were not all consumed): wait, bounded, for
+    // the last load of each slot
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < kQStages; ++i)
+        if (q_last[i] >= 0) mbar_wait(&q_full[i], (uint32_t)(q_last[i] / kQStages) & 1, nullptr);
     }
   } else if (warp == kKVWarp) {
     // -------------------------------------------------- K/V TMA (warp 1)
@@ -313,6 +325,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       const uint64_t pol_kv = l2_policy_evict_first();
       int kv = -1, prev = -1;
+      int k_last[kKVStages], v_last[kKVStages];   // last list loaded into each slot
+#pragma unroll
+      for (int i = 0; i < kKVStages; ++i) k_last[i] = v_last[i] = -1;
       for (int t = 0; t < n && !*abort_flag; ++t) {
         const int4 d = desc[t];
         if (d.x == prev) continue;
@@ -328,12 +343,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int h = 0; h < C::kNHalf; ++h)
           tma_load_3d_hint(smem_u32(sK + ks * C::kSmemK + h * C::kHalf), &tm_k, &k_full[ks], h * 64, g,
                            row, pol_kv);
+        k_last[ks] = kv;
         if (!mbar_wait(&v_empty[ks], (w & 1) ^ 1, a.status)) { *abort_flag = 1; break; }
         mbar_arrive_expect_tx(&v_full[ks], C::kSmemK);
 #pragma unroll
         for (int h = 0; h < C::kNHalf; ++h)
           tma_load_3d_hint(smem_u32(sV + ks * C::kSmemK + h * C::kHalf), &tm_v, &v_full[ks], h * 64, g,
                            row, pol_kv);
+        v_last[ks] = kv;
+      }
+      // as for Q: no copy may still be landing when the CTA exits
+#pragma unroll
+      for (int i = 0; i < kKVStages; ++i) {
+        if (k_last[i] >= 0) mbar_wait(&k_full[i], (uint32_t)(k_last[i] / kKVStages) & 1, nullptr);
+        if (v_last[i] >= 0) mbar_wait(&v_full[i], (uint32_t)(v_last[i] / kKVStages) & 1, nullptr);
       }
     }
   } else if (warp == kMmaWarp) {
