@@ -286,21 +286,29 @@ def time_e2e(job, steps, world):
     out_h = torch.empty(job.out.shape, dtype=torch.int16, pin_memory=True)
     h2d = sum(host[n].numel() * 2 for n in names)
     d2h = sel_h.numel() * 4 + out_h.numel() * 2
-    torch.cuda.synchronize()
-    barrier(world)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    if job.w["kind"] != "decode" and len(job.calls) > 1 and job.B == 1:
+    pipelined = job.w["kind"] != "decode" and len(job.calls) > 1 and job.B == 1
+    if pipelined:
+        comp = torch.cuda.current_stream()
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def run(n):
+        if not pipelined:
+            for _ in range(n):
+                for nm in names:
+                    job.dev[nm].copy_(host[nm], non_blocking=True)
+                job.step()
+                sel_h.copy_(job.sel, non_blocking=True)
+                out_h.copy_(job.out, non_blocking=True)
+            return
         # chunked prefill, pipelined as a caller of the C ABI would run it:
         # chunk c's inputs (its q_idx and q rows, the k_idx rows and K/V blocks
         # of its own 8192 tokens) go up on one stream, its call runs on the
         # compute stream once they have landed, and its out and sel rows come
         # back on a third stream while the next chunk computes.  The same
         # bytes move as in the serial form; only their overlap differs.
-        comp = torch.cuda.current_stream()
-        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-        t0.record(comp)
-        for _ in range(steps):
+        for _ in range(n):
             s_in.wait_stream(comp)      # steps do not overlap
             for c in job.calls:
                 a, T, st = c["qoff"], c["T"], c["q_start"][0]
@@ -323,16 +331,13 @@ def time_e2e(job, steps, world):
                     sel_h[:, a:a + T].copy_(job.sel[:, a:a + T], non_blocking=True)
                     out_h[:, a:a + T].copy_(job.out[:, a:a + T], non_blocking=True)
             comp.wait_stream(s_out)
-        t1.record(comp)
-    else:
-        t0.record()
-        for _ in range(steps):
-            for n in names:
-                job.dev[n].copy_(host[n], non_blocking=True)
-            job.step()
-            sel_h.copy_(job.sel, non_blocking=True)
-            out_h.copy_(job.out, non_blocking=True)
-        t1.record()
+
+    run(1)                              # untimed warm-up of the copy path
+    torch.cuda.synchronize()
+    barrier(world)
+    t0.record()
+    run(steps)
+    t1.record()
     torch.cuda.synchronize()
     ms = max_over_ranks(t0.elapsed_time(t1), world) / steps
     return ms, h2d, d2h
