@@ -327,7 +327,8 @@ __global__ void __launch_bounds__(128) attn_stream_kernel(
   // the warp's whole 32-token K slice is requested before the first score MMA
   // and before the V copy, which is needed later: twice the bytes in flight of
   // loading K in 16-token halves, and K first in the memory queue (measured
-  // 0.128 -> 0.101 ms on the 64 x 256K decode batch, one CTA fewer per SM)
+  // 0.128 -> 0.101 ms on the 64 x 256K decode batch, although the registers
+  // this holds leave 4 CTAs per SM instead of 6)
   uint4 LL0[2][NU], LL1[2][NU];
 #pragma unroll
   for (int mg = 0; mg < 2; ++mg) {
