@@ -63,6 +63,30 @@ def test_prefill_m2_layout_ragged_tail(msa, ref, kernels):
     assert_close(out, want_out)
 
 
+def spike_keys(k, every=7, shift=5):
+    """Every `every`-th token's K row (all groups) times 2^shift, on bf16 bits.
+
+    k is [B][blocks][128][G][D]. Scaling by a power of two only moves the
+    exponent field, so the spiked keys are exact bf16 values."""
+    k = np.array(k, dtype=np.uint16)
+    tok = np.arange(k.shape[1] * k.shape[2]).reshape(1, k.shape[1], k.shape[2], 1, 1)
+    hit = (tok % every == 3) & ((k & 0x7F80) != 0)
+    return np.where(hit, k + np.uint16(shift << 7), k).astype(np.uint16)
+
+
+@pytest.mark.parametrize("kernels", KERNELS)
+def test_spiked_keys_spread_the_scores(msa, ref, kernels):
+    # keys 32x larger at every 7th token spread a block's scaled scores over
+    # about a hundred powers of two: the softmax maximum is far from most
+    # scores, most weights underflow, and each output follows few values
+    wl = Workload(B=1, T=2500, H=48, G=8, D=128, Di=64, ctx=[2500], q_start=[0])
+    wl.k = spike_keys(wl.k)
+    want_sel, want_out = wl.oracle(ref)
+    sel, out = run_forward(msa, wl, kernels)
+    assert_sel_equal(sel, want_sel)
+    assert_close(out, want_out)
+
+
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("H,G", [(4, 4), (8, 4), (12, 4), (20, 4), (48, 8), (28, 4), (32, 4),
                                  (40, 4), (48, 4), (64, 4), (16, 1)])
