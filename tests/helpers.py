@@ -15,8 +15,10 @@ class Workload:
     q_start[b], T: the call's queries are positions q_start[b] .. q_start[b]+T-1.
     """
 
-    def __init__(self, B, T, H, G, D, Di, ctx, q_start, max_blocks=None, seed=syn.BASE_SEED):
+    def __init__(self, B, T, H, G, D, Di, ctx, q_start, max_blocks=None, seed=syn.BASE_SEED,
+                 scale=None):
         self.B, self.T, self.H, self.G, self.D, self.Di = B, T, H, G, D, Di
+        self.scale = scale      # softmax scale; None is 1/sqrt(D)
         self.ctx = [int(c) for c in ctx]
         self.q_start = [int(s) for s in q_start]
         self.kv_len = [self.q_start[b] + T for b in range(B)]
@@ -35,11 +37,11 @@ class Workload:
                            for b in range(B)])
 
     def dims(self, ref):
-        return ref.dims(self.H, self.G, self.D, self.Di)
+        return ref.dims(self.H, self.G, self.D, self.Di, scale=self.scale)
 
     def params(self, msa, kernels="auto"):
         return msa.params(self.B, self.T, self.H, self.G, self.D, self.Di, self.max_blocks,
-                          kernels=kernels)
+                          scale=self.scale, kernels=kernels)
 
     def device(self):
         import torch

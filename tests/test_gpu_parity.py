@@ -87,6 +87,19 @@ def test_spiked_keys_spread_the_scores(msa, ref, kernels):
     assert_close(out, want_out)
 
 
+@pytest.mark.parametrize("kernels", KERNELS)
+@pytest.mark.parametrize("scale", [-0.0625, 0.25])
+def test_caller_scale_of_either_sign(msa, ref, kernels, scale):
+    # the softmax scale is the caller's: with a negative one the largest scaled
+    # score comes from the smallest raw score
+    wl = Workload(B=1, T=1500, H=12, G=4, D=128, Di=64, ctx=[700 + 1500], q_start=[700],
+                  scale=scale)
+    want_sel, want_out = wl.oracle(ref)
+    sel, out = run_forward(msa, wl, kernels)
+    assert_sel_equal(sel, want_sel)
+    assert_close(out, want_out)
+
+
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("H,G", [(4, 4), (8, 4), (12, 4), (20, 4), (48, 8), (28, 4), (32, 4),
                                  (40, 4), (48, 4), (64, 4), (16, 1)])
@@ -143,7 +156,9 @@ def test_unaligned_starts_in_several_sequences(msa, ref, kernels):
 
 @pytest.mark.parametrize("kernels", KERNELS)
 def test_long_context_chunk_spans_several_splits(msa, ref, kernels):
-    # lb up to 312: the tensor-core scan splits the key range (256 blocks per split)
+    # lb up to 312: the streaming scan splits the key range into 64-block
+    # splits (the tensor-core scan's 1024-block splits are crossed at full
+    # size, by the 1M chunked prefill of the full-size tests)
     L = 40000
     wl = Workload(B=1, T=1000, H=4, G=2, D=64, Di=64, ctx=[L], q_start=[L - 1000])
     want_sel, want_out = wl.oracle(ref)
