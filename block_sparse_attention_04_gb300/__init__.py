@@ -14,7 +14,7 @@ from . import _build
 
 __all__ = ["MsaParams", "MsaError", "params", "load", "msa_workspace_bytes", "msa_index_topk",
            "msa_sparse_attn", "msa_forward", "msa_workspace_status", "msa_status_string",
-           "msa_kernel_launch_count", "msa_index_topk_noalloc",
+           "msa_kernel_launch_count", "msa_index_topk_noalloc", "msa_debug_set_wait_polls",
            "workspace", "BLOCK", "TOPK"]
 
 BLOCK = 128
@@ -22,7 +22,7 @@ TOPK = 16
 KERNELS = {"auto": 0, "streaming": 1, "tensorcore": 2}
 EXPORTS = ("msa_workspace_bytes", "msa_index_topk", "msa_sparse_attn", "msa_forward",
            "msa_workspace_status", "msa_status_string", "msa_kernel_launch_count",
-           "msa_index_topk_noalloc")
+           "msa_index_topk_noalloc", "msa_debug_set_wait_polls")
 
 
 class MsaError(RuntimeError):
@@ -65,12 +65,14 @@ def load(path=None):
     L.msa_forward.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, sz, P]
     L.msa_workspace_status.argtypes = [P, P]
     L.msa_index_topk_noalloc.argtypes = [PP, P, P, P, P, P, P]
+    L.msa_debug_set_wait_polls.argtypes = [ctypes.c_uint32]
+    L.msa_debug_set_wait_polls.restype = None
     L.msa_kernel_launch_count.argtypes = []
     L.msa_kernel_launch_count.restype = ctypes.c_uint64
     L.msa_status_string.argtypes = [ci]
     L.msa_status_string.restype = ctypes.c_char_p
     for f in ("msa_index_topk", "msa_sparse_attn", "msa_forward", "msa_workspace_status",
-              "msa_index_topk_noalloc"):
+              "msa_index_topk_noalloc", "msa_debug_set_wait_polls"):
         getattr(L, f).restype = ci
     if path == _build.LIBMSA:
         _lib = L
@@ -105,6 +107,12 @@ def _host_i32(x, B):
 
 def msa_kernel_launch_count():
     return int(load().msa_kernel_launch_count())
+
+
+def msa_debug_set_wait_polls(polls):
+    """Test-only: cap the tensor-core kernels' pipeline waits at `polls` polls
+    (0 restores the default wall-clock bound)."""
+    load().msa_debug_set_wait_polls(int(polls))
 
 
 def msa_workspace_bytes(p):

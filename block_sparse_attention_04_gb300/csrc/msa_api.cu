@@ -14,6 +14,9 @@ namespace msa {
 static std::atomic<uint64_t> g_launches{0};
 void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+static std::atomic<uint32_t> g_wait_polls{0};
+uint32_t debug_wait_polls() { return g_wait_polls.load(std::memory_order_relaxed); }
+
 constexpr int kMaxContextBlocks = 32768;
 
 int validate_params(const msa_params* p) {
@@ -245,11 +248,15 @@ int msa_workspace_status(const void* ws, cudaStream_t stream) {
   int v = 0;
   if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MSA_ERR_CUDA;
   if (v == kDevTimeout) return MSA_ERR_TIMEOUT;
-  if (v == 2) return MSA_ERR_INVALID_ARG;
+  if (v == kDevInvalid) return MSA_ERR_INVALID_ARG;
   return v == 0 ? MSA_OK : MSA_ERR_CUDA;
 }
 
 uint64_t msa_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void msa_debug_set_wait_polls(uint32_t polls) {
+  g_wait_polls.store(polls, std::memory_order_relaxed);
+}
 
 const char* msa_status_string(int status) {
   switch (status) {

@@ -55,6 +55,7 @@ struct AttnPass {
   uint16_t* part_o;      // [B*Tp*H*16][D] bf16, O = sum 2^(s-m) v (unnormalised)
   float2* part_ml;       // [B*Tp*H*16] (m in log2 units, l)
   int* status;
+  uint32_t wait_polls;   // poll cap of the pipeline waits (0: wall-clock bound only)
 };
 
 __device__ __forceinline__ bool slot_valid(const AttnPass& a, int b, int i, int kb) {
@@ -75,7 +76,7 @@ __global__ void csr_count_kernel(AttnPass a) {
     const int kb = a.sel[(((size_t)b * a.s.T + i) * a.s.G + g) * kTopk + j];
     if (kb < 0) continue;
     if (!slot_valid(a, b, i, kb)) {
-      atomicExch(a.status, 2);
+      flag_invalid(a.status);
       continue;
     }
     atomicAdd(&a.count[((size_t)b * a.nbl + kb) * a.s.G + g], 1);
@@ -188,24 +189,6 @@ struct AttnCfg {
   static constexpr uint32_t kTmemCols = 512;
 };
 
-// Maximum / minimum of 16 fp32 values held as raw bits (3-input trees).
-__device__ __forceinline__ float tree_max16(const uint32_t (&v)[16]) {
-  float t[5];
-#pragma unroll
-  for (int k = 0; k < 5; ++k)
-    t[k] = fmax3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]),
-                 __uint_as_float(v[3 * k + 2]));
-  return fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], __uint_as_float(v[15])), -INFINITY);
-}
-__device__ __forceinline__ float tree_min16(const uint32_t (&v)[16]) {
-  float t[5];
-#pragma unroll
-  for (int k = 0; k < 5; ++k)
-    t[k] = fmin3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]),
-                 __uint_as_float(v[3 * k + 2]));
-  return fmin3(fmin3(t[0], t[1], t[2]), fmin3(t[3], t[4], __uint_as_float(v[15])), INFINITY);
-}
-
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -288,6 +271,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
     for (int i = 0; i < kQStages; ++i) q_last[i] = -1;
     for (int t = 0; t < n; ++t) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // warp-uniform
       const int4 d = desc[t];
       const int ne = d.z;
       int qrow = 0;
@@ -298,7 +282,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       const int qs = t % kQStages;
       const uint32_t u = (uint32_t)(t / kQStages);
-      if (!__all_sync(0xffffffffu, mbar_wait(&q_empty[qs], (u & 1) ^ 1, a.status))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&q_empty[qs], (u & 1) ^ 1, a.status, a.wait_polls))) {
         *abort_flag = 1;
         break;
       }
@@ -337,14 +321,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t w = (uint32_t)(kv / kKVStages);
         const int kb = d.w & 0x7FFF, g = (d.w >> 15) & 7, b = d.w >> 18;
         const int row = (int)(((int64_t)b * a.s.max_blocks + kb) * kBlock);
-        if (!mbar_wait(&k_empty[ks], (w & 1) ^ 1, a.status)) { *abort_flag = 1; break; }
+        if (!mbar_wait(&k_empty[ks], (w & 1) ^ 1, a.status, a.wait_polls)) { *abort_flag = 1; break; }
         mbar_arrive_expect_tx(&k_full[ks], C::kSmemK);
 #pragma unroll
         for (int h = 0; h < C::kNHalf; ++h)
           tma_load_3d_hint(smem_u32(sK + ks * C::kSmemK + h * C::kHalf), &tm_k, &k_full[ks], h * 64, g,
                            row, pol_kv);
         k_last[ks] = kv;
-        if (!mbar_wait(&v_empty[ks], (w & 1) ^ 1, a.status)) { *abort_flag = 1; break; }
+        if (!mbar_wait(&v_empty[ks], (w & 1) ^ 1, a.status, a.wait_polls)) { *abort_flag = 1; break; }
         mbar_arrive_expect_tx(&v_full[ks], C::kSmemK);
 #pragma unroll
         for (int h = 0; h < C::kNHalf; ++h)
@@ -392,8 +376,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           w = (uint32_t)(kv / kKVStages);
           last = (t + 1 == n) || ln != lt;
           const int c = t & 1, qs = t % kQStages;
-          ok = mbar_wait(&q_full[qs], (uint32_t)(t / kQStages) & 1, a.status) &&
-               (!first || mbar_wait(&k_full[ks], w & 1, a.status));
+          ok = mbar_wait(&q_full[qs], (uint32_t)(t / kQStages) & 1, a.status, a.wait_polls) &&
+               (!first || mbar_wait(&k_full[ks], w & 1, a.status, a.wait_polls));
           if (!ok) break;
           tc_fence_after();
           const uint32_t q0 = smem_u32(sQ + qs * C::kSmemQ), k0 = smem_u32(sK + ks * C::kSmemK);
@@ -413,9 +397,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           // ---- P.V(t - 1)
           const int tp = t - 1, c = tp & 1;
           const uint32_t j = (uint32_t)(tp >> 1);
-          ok = mbar_wait(&p_full[c], j & 1, a.status) &&
-               (!pv_first || mbar_wait(&v_full[pv_ks], pv_w & 1, a.status)) &&
-               (j == 0 || mbar_wait(&o_empty[c], (j - 1) & 1, a.status));
+          ok = mbar_wait(&p_full[c], j & 1, a.status, a.wait_polls) &&
+               (!pv_first || mbar_wait(&v_full[pv_ks], pv_w & 1, a.status, a.wait_polls)) &&
+               (j == 0 || mbar_wait(&o_empty[c], (j - 1) & 1, a.status, a.wait_polls));
           if (!ok) break;
           tc_fence_after();
           const uint32_t v0 = smem_u32(sV + pv_ks * C::kSmemK);
@@ -445,7 +429,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + c * 128;
     const float sl = a.s.scale * kLog2e;
     for (int t = c; t < n; t += 2) {
-      if (*abort_flag) break;
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // warp-uniform
       const int4 d = desc[t];
       const int kb = d.w & 0x7FFF, g = (d.w >> 15) & 7, b = d.w >> 18;
       const int e = r >> rshift, hh = r & (a.rpe - 1);
@@ -460,7 +444,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // tokens kb*128 + col with col > lim are masked (only in the local block)
       const int lim = (int)(tq - (int64_t)kb * kBlock);
       const bool masked = __any_sync(0xffffffffu, valid && lim < kBlock - 1);
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[c], (uint32_t)(t >> 1) & 1, a.status))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[c], (uint32_t)(t >> 1) & 1, a.status, a.wait_polls))) {
         *abort_flag = 1;
         break;
       }
@@ -474,10 +458,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float mx = neg ? INFINITY : -INFINITY;
 #pragma unroll 1
       for (int cc = 0; cc < 8; ++cc) {
-        uint32_t h[16];
-        tmem_ld16(lane_base + cc * 16, h);
-        tmem_ld_wait();
         if (masked) {
+          uint32_t h[16];
+          tmem_ld16(lane_base + cc * 16, h);
+          tmem_ld_wait();
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
             const float x = __uint_as_float(h[k]);
@@ -485,7 +469,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mx = neg ? fminf(mx, in ? x : INFINITY) : fmaxf(mx, in ? x : -INFINITY);
           }
         } else {
-          mx = neg ? fminf(mx, tree_min16(h)) : fmaxf(mx, tree_max16(h));
+          // the load reduces the 16 scores itself
+          if (neg) {
+            const float r = tmem_ld16_red<false>(lane_base + cc * 16);
+            tmem_ld_wait();
+            mx = fminf(mx, r);
+          } else {
+            const float r = tmem_ld16_red<true>(lane_base + cc * 16);
+            tmem_ld_wait();
+            mx = fmaxf(mx, r);
+          }
         }
       }
       const float m = mx * sl;
@@ -541,7 +534,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int r = quad * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + 256 + c * 128;
     for (int t = c; t < n; t += 2) {
-      if (*abort_flag) break;
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // warp-uniform
       const int4 d = desc[t];
       const int g = (d.w >> 15) & 7, b = d.w >> 18;
       const int e = r >> rshift, hh = r & (a.rpe - 1);
@@ -551,7 +544,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int en = a.entries[d.y + e];
         prow = (((size_t)b * a.Tp + (en >> 4)) * H + (size_t)g * hpg + hh) * kTopk + (en & 15);
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(&o_full[c], (uint32_t)(t >> 1) & 1, a.status))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&o_full[c], (uint32_t)(t >> 1) & 1, a.status, a.wait_polls))) {
         *abort_flag = 1;
         break;
       }
@@ -725,6 +718,7 @@ cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint
     a.part_o = reinterpret_cast<uint16_t*>(base + lay.po_off);
     a.part_ml = reinterpret_cast<float2*>(base + lay.pml_off);
     a.status = ws.status;
+    a.wait_polls = debug_wait_polls();
     if ((e = cudaMemsetAsync(a.count, 0, (size_t)a.nlists * 4, st)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(a.cursor, 0, (size_t)a.nlists * 4, st)) != cudaSuccess) return e;
     const int64_t n = (int64_t)s.B * a.Tp * s.G * kTopk;

@@ -134,22 +134,31 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Bounded wait: polls for at most kWaitNs of wall time.  On expiry it records
-// kDevTimeout in the status word (if given) and returns false; the caller then
-// stops issuing work and drains.  Every legitimate wait in these kernels lasts
-// microseconds.
+// Bounded wait: polls for at most kWaitNs of wall time and, when max_polls is
+// nonzero, for at most max_polls polls after the first (a shorter bound that
+// only tests of the failure path set, on pipeline waits).  On expiry it
+// records kDevTimeout in the status word (if given) and returns false; the
+// caller then stops issuing work and drains.  Every legitimate wait in these
+// kernels lasts microseconds.  Drain waits (copies or MMAs already issued,
+// which complete by themselves) always keep the wall-clock bound alone.
 constexpr uint64_t kWaitNs = 2000000000ull;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          uint32_t max_polls = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitNs) {
+    if ((max_polls != 0 && i >= max_polls) ||
+        ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitNs)) {
       if (status) atomicExch(status, (int)kDevTimeout);
       return false;
     }
   }
 }
+
+// Records an invalid selected id in the status word unless a timeout (which
+// takes precedence) is already recorded.
+__device__ __forceinline__ void flag_invalid(int* status) { atomicCAS(status, 0, kDevInvalid); }
 
 // --------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void tma_load_2d(uint32_t sdst, const void* tmap, uint64_t* bar,
@@ -248,6 +257,35 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
+}
+// The maximum (MAX) or minimum of each lane's 16 consecutive fp32 columns,
+// reduced by the load itself (sm_103a's reducing form of tcgen05.ld, 32 lanes
+// x 16 columns).  The loaded values themselves are not returned.  No wait:
+// the reduction is valid after tcgen05.wait::ld.
+template <bool MAX>
+__device__ __forceinline__ float tmem_ld16_red(uint32_t taddr) {
+  float red;
+  uint32_t r[16];
+#define MSA_LDRED(OP)                                                                        \
+  asm volatile(                                                                              \
+      "tcgen05.ld.red.sync.aligned.32x32b.x16." OP ".f32 "                                   \
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, %16, [%17];"                 \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),           \
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=f"(red)                                     \
+      : "r"(taddr))
+  if constexpr (MAX) {
+    MSA_LDRED("max");
+  } else {
+    MSA_LDRED("min");
+  }
+#undef MSA_LDRED
+  // an empty statement that takes the 16 values, so that their registers are
+  // released here like any consumed value (no instruction is emitted)
+  asm volatile("" ::"r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+               "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+               "r"(r[13]), "r"(r[14]), "r"(r[15]));
+  return red;
 }
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
 #define MSA_R(i) "=r"(r[i])

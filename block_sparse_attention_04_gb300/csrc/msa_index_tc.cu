@@ -15,8 +15,9 @@
 //               into one of two TMEM accumulator stages;
 //   warps 2-17  epilogue, four warpgroups: two read each accumulator stage
 //               (one key block each), stages alternate between the two
-//               pairs; tcgen05.ld of the row's 128 fp32 scores in 16-column
-//               chunks, block maximum (3-input max), insertion into a
+//               pairs; reducing tcgen05.ld of the row's 128 fp32 scores in
+//               16-column chunks (the load returns each chunk's maximum),
+//               block maximum, insertion into a
 //               register-resident top-15 (score desc, block id asc); the four
 //               lists merge through shared memory at the end of the item.
 // The [query x block] score matrix never leaves TMEM/registers.  Each item
@@ -63,15 +64,18 @@ struct IndexTcArgs {
   int npairs;         // row tiles per sequence
   int nsplit;         // splits per row tile (the merge's list count per row)
   int64_t cap;        // K_idx rows per sequence
-  const int32_t* items;  // packed (b, tile, split), heaviest first
+  const int2* items;     // (row tile, b << 7 | split), heaviest first
   const int32_t* nitems;
   Cand* cand;
   int* status;
+  uint32_t wait_polls;   // poll cap of the pipeline waits (0: wall-clock bound only)
 };
 
-// packed work item: split (7 bits) | b (8 bits) | row tile (17 bits)
-__host__ __device__ __forceinline__ int32_t pack_item(int b, int p, int sp) {
-  return (int32_t)(((uint32_t)p << 15) | ((uint32_t)b << 7) | (uint32_t)sp);
+// A work item: the row tile in a word of its own (it reaches T*G/128, which
+// the host bounds only by T*G < 2^31), then the sequence (8 bits, B <= 256)
+// and the split (7 bits, at most 32 splits of 1024 blocks).
+__host__ __device__ __forceinline__ int2 pack_item(int b, int p, int sp) {
+  return make_int2(p, (b << 7) | sp);
 }
 
 __device__ __forceinline__ int pair_kb_end(const Shape& s, const Positions& pos, int b, int p) {
@@ -82,7 +86,7 @@ __device__ __forceinline__ int pair_kb_end(const Shape& s, const Positions& pos,
 // Dense list of the work items that have key blocks, heaviest first: row
 // tiles in descending order (their key ranges grow), each tile's splits in order.
 __global__ void __launch_bounds__(1024) index_items_kernel(Shape s, Positions pos, int npairs,
-                                                           int32_t* items, int32_t* nitems) {
+                                                           int2* items, int32_t* nitems) {
   __shared__ int64_t part[1024];
   const int64_t n = (int64_t)s.B * npairs;
   const int64_t per = (n + 1023) / 1024;
@@ -110,11 +114,11 @@ __global__ void __launch_bounds__(1024) index_items_kernel(Shape s, Positions po
   if (threadIdx.x == 1023) *nitems = (int32_t)part[1023];
 }
 
-__device__ __forceinline__ void item_range(const IndexTcArgs& a, int32_t packed, int& b, int& p,
+__device__ __forceinline__ void item_range(const IndexTcArgs& a, int2 packed, int& b, int& p,
                                            int& sp, int& k0, int& k1) {
-  sp = packed & 127;
-  b = (packed >> 7) & 255;
-  p = (int)((uint32_t)packed >> 15);
+  sp = packed.y & 127;
+  b = (packed.y >> 7) & 255;
+  p = packed.x;
   k0 = sp * kSplitBlocks;
   k1 = min(k0 + kSplitBlocks, pair_kb_end(a.s, a.pos, b, p));
 }
@@ -210,17 +214,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0, abuf = 0;
       uint32_t sphase = 0, aphase = 0;
-      int issued = 0;
+      int issued = 0, a_issued = 0;
       for (int it = blockIdx.x; it < nitems && !*abort_flag; it += gridDim.x) {
         int b, p, sp, k0, k1;
         item_range(a, a.items[it], b, p, sp, k0, k1);
-        if (!mbar_wait(&a_empty[abuf], aphase ^ 1, a.status)) { *abort_flag = 1; break; }
+        if (!mbar_wait(&a_empty[abuf], aphase ^ 1, a.status, a.wait_polls)) { *abort_flag = 1; break; }
         mbar_arrive_expect_tx(&a_full[abuf], C::kTileBytes);
         tma_load_2d(smem_u32(sA + abuf * C::kTileBytes), &tm_q, &a_full[abuf], 0,
                     (b * T) * G + p * kItemRows);
+        ++a_issued;
         if (++abuf == 2) { abuf = 0; aphase ^= 1; }
         for (int kb = k0; kb < k1; kb += 2) {
-          if (!mbar_wait(&empty[stage], sphase ^ 1, a.status)) { *abort_flag = 1; break; }
+          if (!mbar_wait(&empty[stage], sphase ^ 1, a.status, a.wait_polls)) { *abort_flag = 1; break; }
           mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
           const uint32_t dst = smem_u32(sB + stage * C::kStageBytes);
           const int row = (int)(b * a.cap + (int64_t)kb * kBlock);
@@ -232,14 +237,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == kStages) { stage = 0; sphase ^= 1; }
         }
       }
-      if (*abort_flag) {
-        // drain: wait (bounded) for the loads this thread issued most recently
+      // No copy may still be landing in shared memory when the CTA exits: wait
+      // (bounded) for the last load issued into each K_idx stage and each
+      // Q_idx buffer.  Without an abort they were all consumed, and the waits
+      // return at once; after one (a wait ran out anywhere in the CTA, maybe
+      // after this loop ended) the consumers may have skipped them.
+      {
         int n = issued < kStages ? issued : kStages;
         int st = stage;
         uint32_t ph = sphase;
         for (int k = 0; k < n; ++k) {
           if (st == 0) { st = kStages - 1; ph ^= 1; } else { --st; }
           mbar_wait(&full[st], ph, nullptr);
+        }
+        n = a_issued < 2 ? a_issued : 2;
+        int ab = abuf;
+        uint32_t aph = aphase;
+        for (int k = 0; k < n; ++k) {
+          if (ab == 0) { ab = 1; aph ^= 1; } else { --ab; }
+          mbar_wait(&a_full[ab], aph, nullptr);
         }
       }
     }
@@ -252,13 +268,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = blockIdx.x; it < nitems && !*abort_flag; it += gridDim.x) {
         int b, p, sp, k0, k1;
         item_range(a, a.items[it], b, p, sp, k0, k1);
-        if (!mbar_wait(&a_full[abuf], aphase, a.status)) { *abort_flag = 1; break; }
+        if (!mbar_wait(&a_full[abuf], aphase, a.status, a.wait_polls)) { *abort_flag = 1; break; }
         tc_fence_after();
         const uint32_t a0 = smem_u32(sA + abuf * C::kTileBytes);
         bool ok = true;
         for (int kb = k0; kb < k1; kb += 2) {
-          if (!mbar_wait(&full[stage], sphase, a.status) ||
-              !mbar_wait(&tm_empty[ts], tphase ^ 1, a.status)) {
+          if (!mbar_wait(&full[stage], sphase, a.status, a.wait_polls) ||
+              !mbar_wait(&tm_empty[ts], tphase ^ 1, a.status, a.wait_polls)) {
             ok = false;
             break;
           }
@@ -318,31 +334,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       // this warpgroup's stages of the item: global index == my_ts (mod 2)
       for (int q = ((my_ts - gstage) & 1); q < nst; q += 2) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&tm_full[my_ts], tphase, a.status))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&tm_full[my_ts], tphase, a.status, a.wait_polls))) { ok = false; break; }
         tphase ^= 1;
         tc_fence_after();
         // eight 16-column loads, each waited before the next is issued: small
         // loads leave the concurrently accumulating MMA more of tensor memory
-        // than larger or overlapped ones (measured)
-        uint32_t v[16];
+        // than larger or overlapped ones (measured).  The load itself reduces
+        // each lane's 16 scores to their maximum, so the block max-pool costs
+        // no ALU work beyond combining eight partial maxima.
         float m = -INFINITY;
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 8; ++c) {
-          tmem_ld16(lane_base + c * 16, v);
+          const float cm = tmem_ld16_red<true>(lane_base + c * 16);
           tmem_ld_wait();
-          if (c == 7) {  // the stage's scores are all in registers
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tm_empty[my_ts]);
-          }
-          const float x0 = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-          const float x1 = fmax3(__uint_as_float(v[3]), __uint_as_float(v[4]), __uint_as_float(v[5]));
-          const float x2 = fmax3(__uint_as_float(v[6]), __uint_as_float(v[7]), __uint_as_float(v[8]));
-          const float x3 = fmax3(__uint_as_float(v[9]), __uint_as_float(v[10]), __uint_as_float(v[11]));
-          const float x4 =
-              fmax3(__uint_as_float(v[12]), __uint_as_float(v[13]), __uint_as_float(v[14]));
-          m = fmax3(m, fmax3(x0, x1, x2), fmax3(x3, x4, __uint_as_float(v[15])));
+          m = fmaxf(m, cm);
         }
+        // the stage's scores are all read: the MMA may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tm_empty[my_ts]);
         const int blk = k0 + 2 * q + half;
         if (valid && blk < k1 && blk < lb && m > sc[kCand - 1]) list_insert_newest(sc, id, m, blk);
       }
@@ -444,7 +454,7 @@ cudaError_t launch_index_tc_impl(const Shape& s, const Positions& pos, const uin
   }
   char* base = reinterpret_cast<char*>(ws.cand);
   int32_t* nitems = reinterpret_cast<int32_t*>(base + cand_bytes(s));
-  int32_t* items = nitems + 64;
+  int2* items = reinterpret_cast<int2*>(nitems + 64);
   IndexTcArgs a;
   a.s = s;
   a.pos = pos;
@@ -455,6 +465,7 @@ cudaError_t launch_index_tc_impl(const Shape& s, const Positions& pos, const uin
   a.nitems = nitems;
   a.cand = ws.cand;
   a.status = ws.status;
+  a.wait_polls = debug_wait_polls();
   cudaError_t e = cudaFuncSetAttribute(index_tc_kernel<DI>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
@@ -471,7 +482,7 @@ cudaError_t launch_index_tc_impl(const Shape& s, const Positions& pos, const uin
 }  // namespace
 
 size_t tc_index_workspace_bytes(const Shape& s) {
-  return cand_bytes(s) + 256 + items_cap(s) * sizeof(int32_t);
+  return cand_bytes(s) + 256 + items_cap(s) * sizeof(int2);
 }
 
 cudaError_t launch_index_tc(const Shape& s, const Positions& pos, const uint16_t* q_idx,

@@ -13,6 +13,11 @@ constexpr int kTopk = MSA_TOPK;       // selected blocks per (query, group)
 constexpr int kCand = MSA_TOPK - 1;   // ranked candidates besides the local block
 constexpr int kMaxBatch = MSA_MAX_BATCH;
 constexpr int kDevTimeout = 1;        // status word value: a bounded wait ran out
+constexpr int kDevInvalid = 2;        // status word value: a selected id out of range
+
+// Poll cap of the kernels' pipeline waits (0: the wall-clock bound alone);
+// set only through msa_debug_set_wait_polls.
+uint32_t debug_wait_polls();
 
 // Adds n to the library-wide count of enqueued kernels.
 void note_launches(int n);

@@ -8,6 +8,8 @@
 // msa_index_topk needs either.  This entry point keeps its scratch (the
 // per-split candidate lists) in a file-scope __device__ array instead, so it
 // allocates nothing and needs no workspace argument.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "msa_internal.h"
@@ -22,23 +24,77 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MSA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::mutex g_setup_mu;
-void* g_scratch_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
 
-// Set-up, once per device, with that device current: look up the device
-// address of the scratch array.  The first call on each device does this.
+// The array's device address, looked up once per device and remembered with
+// the id of the context it was looked up in.  The module (and so the array)
+// belongs to a context: after cudaDeviceReset, or under another context on
+// the same device, the id differs and the address is looked up again.
+struct ScratchSlot {
+  unsigned long long ctx_id;
+  void* addr;
+};
+std::mutex g_setup_mu;
+ScratchSlot g_slots[kMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// The driver's context calls, looked up through the runtime (libmsa does not
+// link the driver library directly).
+bool driver_ctx_calls(CtxGetCurrentFn* cur, CtxGetIdFn* id) {
+  static CtxGetCurrentFn f_cur = nullptr;
+  static CtxGetIdFn f_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      f_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      f_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  *cur = f_cur;
+  *id = f_id;
+  return f_cur && f_id;
+}
+
+// Id of the calling thread's current context, 0 if there is none yet.
+int current_ctx_id(unsigned long long* out) {
+  CtxGetCurrentFn cur;
+  CtxGetIdFn id;
+  if (!driver_ctx_calls(&cur, &id)) return MSA_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (cur(&ctx) != CUDA_SUCCESS) return MSA_ERR_CUDA;
+  *out = 0;
+  if (ctx && id(ctx, out) != CUDA_SUCCESS) return MSA_ERR_CUDA;
+  return MSA_OK;
+}
+
+// Set-up, once per device (and again if that device's context changed), with
+// that device current: look up the device address of the scratch array.  The
+// first call on each device does this.
 int scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return MSA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MSA_ERR_UNSUPPORTED;
+  unsigned long long ctx = 0;
+  int rc = current_ctx_id(&ctx);
+  if (rc) return rc;
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchSlot& slot = g_slots[dev];
+  if (ctx == 0 || slot.addr == nullptr || slot.ctx_id != ctx) {
     void* addr = nullptr;
+    // makes the device's primary context current if the thread had none
     if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
       return MSA_ERR_CUDA;
-    g_scratch_addr[dev] = addr;
+    if ((rc = current_ctx_id(&ctx))) return rc;
+    slot.ctx_id = ctx;
+    slot.addr = addr;
   }
-  *out = g_scratch_addr[dev];
+  *out = slot.addr;
   return MSA_OK;
 }
 

@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(128) attn_stream_kernel(
 
   int kb = sel[((size_t)(b * T + i) * G + g) * kTopk + slot];
   if (kb > lb || kb >= s.max_blocks) {
-    if (threadIdx.x == 0) atomicExch(status, 2);
+    if (threadIdx.x == 0) flag_invalid(status);
     kb = -1;
   }
   if (kb < 0) {

@@ -139,10 +139,15 @@ int msa_forward(const msa_params *p, const uint16_t *q_idx, const uint16_t *k_id
  * array of MSA_NOALLOC_SCRATCH_BYTES bytes inside the library, which every
  * GPU that loads the library holds until the process exits.
  *   - Same arguments and results as msa_index_topk (sel is bit-identical),
- *     minus ws/ws_bytes.  The stream must belong to the current device.
+ *     minus ws/ws_bytes, except that p->kernels is ignored: this entry point
+ *     always runs the streaming (per-query) index kernels, whichever family
+ *     p->kernels names.  The stream must belong to the current device.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current, and remembers it with
+ *     the id of the current CUDA context; a call under another context of
+ *     that device (after cudaDeviceReset, for example) looks it up again.
+ *     Make the first call on a device (and the first after a reset) before
+ *     any stream capture.
  *   - Returns MSA_ERR_WORKSPACE when the call would need more scratch than
  *     MSA_NOALLOC_SCRATCH_BYTES (B*T*ceil(max lb/64)*G*15*8 bytes, splits
  *     capped at 128), MSA_ERR_UNSUPPORTED when B*T > 65535.
@@ -156,9 +161,10 @@ int msa_index_topk_noalloc(const msa_params *p, const uint16_t *q_idx, const uin
 
 /* Waits for `stream`, then returns the status the last call on ws left in
  * it: MSA_OK; MSA_ERR_TIMEOUT if a kernel's bounded wait ran out (its
- * outputs are then incomplete); MSA_ERR_INVALID_ARG if msa_sparse_attn met
- * a selected id outside [0, lb] or beyond max_blocks (that id was skipped,
- * never read).  MSA_ERR_CUDA if the read itself fails. */
+ * outputs are then incomplete; this takes precedence over the next case);
+ * MSA_ERR_INVALID_ARG if msa_sparse_attn met a selected id outside [0, lb]
+ * or beyond max_blocks (that id was skipped, never read).  MSA_ERR_CUDA if
+ * the read itself fails. */
 int msa_workspace_status(const void *ws, cudaStream_t stream);
 
 /* A static, human-readable name of a status code. */
@@ -168,6 +174,19 @@ const char *msa_status_string(int status);
  * loaded (all threads, all devices).  Benchmarks read it before and after a
  * timed region to count the launches inside it. */
 uint64_t msa_kernel_launch_count(void);
+
+/* Diagnostics, for tests of the failure path only (the pages have no
+ * counterpart).  Every wait of a tensor-core kernel's pipeline (a stage
+ * awaited from another warp: a copy landing, an MMA done, a buffer freed) is
+ * bounded by 2 s of wall-clock time; on expiry the kernel records
+ * MSA_ERR_TIMEOUT in ws, stops issuing work, waits for the copies and MMAs it
+ * already issued (these waits keep the 2 s bound alone, so nothing lands in
+ * shared memory after the CTA exits and tensor memory is always released)
+ * and exits.  With polls > 0, each pipeline wait also gives up after `polls`
+ * unsuccessful polls, so that a test can make the timeout happen on a correct
+ * kernel; 0 (the default) restores the wall-clock bound alone.  Applies to
+ * launches made after the call, from any thread; not for production use. */
+void msa_debug_set_wait_polls(uint32_t polls);
 
 #ifdef __cplusplus
 }

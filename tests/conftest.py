@@ -18,3 +18,20 @@ def ref():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(autouse=True)
+def _name_error_stats(request):
+    from tests import helpers
+    helpers.CURRENT_TEST[0] = request.node.nodeid
+    yield
+
+
+def pytest_terminal_summary(terminalreporter):
+    from tests import helpers
+    if not helpers.ERRSTATS:
+        return
+    tr = terminalreporter
+    tr.section("output error against the oracle (tolerance max 2e-2, mean 2e-3)")
+    for name, mx, mean, n in helpers.ERRSTATS:
+        tr.write_line("%-90s max|err| %.3e  mean|err| %.3e  (%d values)" % (name, mx, mean, n))

@@ -7,6 +7,15 @@ import msa_synth as syn
 MAX_ABS = 2e-2      # tolerance on outputs (bf16 in, fp32 accumulate, bf16 out)
 MEAN_ABS = 2e-3
 
+# (test id, max|err|, mean|err|, compared values) of every output comparison
+# in this session; the terminal summary prints them (tests/conftest.py)
+ERRSTATS = []
+CURRENT_TEST = [""]
+
+
+def record_err(err):
+    ERRSTATS.append((CURRENT_TEST[0], float(err.max()), float(err.mean()), int(err.size)))
+
 
 class Workload:
     """Host (numpy, bf16 bits) inputs of B sequences.
@@ -85,6 +94,7 @@ def bf16_to_f64(a):
 def assert_close(got, want, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
     assert np.all(np.isfinite(got)), "non-finite outputs (unwritten rows?)"
     err = np.abs(got - want)
+    record_err(err)
     assert err.max() <= max_abs and err.mean() <= mean_abs, (
         "max|err| %.4g (tol %.1g), mean|err| %.4g (tol %.1g)" % (err.max(), max_abs, err.mean(),
                                                                  mean_abs))

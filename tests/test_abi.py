@@ -146,3 +146,35 @@ def test_forward_and_attn_validate_pointers(lib):
     assert L.msa_sparse_attn(ctypes.byref(p), a, a, a, a, qs, kl, a, a, n, None) == OK
     assert L.msa_sparse_attn(ctypes.byref(p), a, a, a, None, qs, kl, a, a, n, None) == INVALID
     assert L.msa_sparse_attn(ctypes.byref(p), a, a, a, a, None, kl, a, a, n, None) == INVALID
+
+
+def test_noalloc_rejects_calls_beyond_its_scratch(lib):
+    # 256 sequences x 4M-token contexts need 256*128*8*15*8 bytes of candidate
+    # lists, more than the static 16 MiB: rejected on the host, before any
+    # CUDA call (the pointers are never dereferenced)
+    p = msa.params(256, 1, 48, 8, 128, 64, 32768)
+    qs = [32768 * 128 - 1] * 256
+    kl = [32768 * 128] * 256
+    with pytest.raises(msa.MsaError) as e:
+        msa.msa_index_topk_noalloc(p, 0x10000, 0x20000, qs, kl, 0x30000, stream=0)
+    assert e.value.status == WORKSPACE
+    p = msa.params(300, 1, 48, 8, 128, 64, 4)                  # B beyond MSA_MAX_BATCH
+    with pytest.raises(msa.MsaError) as e:
+        msa.msa_index_topk_noalloc(p, 0x10000, 0x20000, [0] * 300, [1] * 300, 0x30000,
+                                   stream=0)
+    assert e.value.status == UNSUPPORTED
+
+
+def test_large_single_prefill_call_is_accepted(lib):
+    # T*G above 2^24 (query, group) rows in one call: more than 2^17 row
+    # tiles of the tensor-core index scan.  The host accepts the shape and
+    # sizes the workspace for every row (the parity of such a call is a GPU
+    # test); the positions check still applies.
+    T = (1 << 21) + 700
+    nb = (T + 127) // 128
+    p = msa.params(1, T, 8, 8, 64, 64, nb, kernels="tensorcore")
+    n = msa.msa_workspace_bytes(p)
+    cand = T * ((nb - 1 + 1023) // 1024) * 8 * 15 * 8     # per-split top-15 lists
+    assert n >= cand + T * 8 * 16 * 4
+    assert call_index(p, q_start=(0,), kv_len=(T,), ws_bytes=n - 1) == WORKSPACE
+    assert call_index(p, q_start=(1,), kv_len=(T,), ws_bytes=n) == INVALID

@@ -77,3 +77,21 @@ def test_decode_bytes_match_a_counted_gather(ref):
     small = bench.H * D * 2 * 2 + G * Di * 2 + G * 16 * 4
     assert got_kidx == kidx_bytes
     assert got_rest == kv_bytes + small
+
+
+def test_recorded_traffic_is_null_once_the_kernel_sources_change(tmp_path, monkeypatch):
+    # roofline.traffic comes from a recorded capture that carries a hash of
+    # the kernel sources it was taken on; a capture of other sources is not
+    # reported, and the recorded bytes scale with the units of the launch
+    import json
+    import bench
+    f = tmp_path / "traffic.json"
+    sha = bench.kernel_sources_sha("index_tc")
+    f.write_text(json.dumps({"index_tc": {"sources_sha": sha, "dram_bytes": 1000.0,
+                                          "units": 10.0}}))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.recorded_traffic("index_tc", 25.0) == 2500.0
+    assert bench.recorded_traffic("index_stream", 25.0) is None
+    f.write_text(json.dumps({"index_tc": {"sources_sha": "0" * 16, "dram_bytes": 1000.0,
+                                          "units": 10.0}}))
+    assert bench.recorded_traffic("index_tc", 25.0) is None

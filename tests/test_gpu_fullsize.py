@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import msa_synth as syn
-from tests.helpers import MAX_ABS, MEAN_ABS, bf16_to_f64
+from tests.helpers import MAX_ABS, MEAN_ABS, bf16_to_f64, record_err
 
 pytestmark = pytest.mark.gpu
 
@@ -71,6 +71,7 @@ def check_rows(ref, job, rows, kidx, attn_rows=None, kv=None):
     err = np.concatenate([
         np.abs(bf16_to_f64(job.out[b, t - base].cpu().numpy()) - w).reshape(-1)
         for (b, t), w in zip(attn_rows, wants)])
+    record_err(err)
     assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (err.max(), err.mean())
     return err.max(), err.mean()
 
@@ -102,14 +103,36 @@ def test_prefill_32k_all_selections(ref):
     q_idx = syn.qidx_rows(job.seed, 0, 0, L, G, DI)[None]
     want = ref.index_topk(d, q_idx, kidx[0][None], 0, L, L // BLK)
     assert np.array_equal(job.sel.cpu().numpy(), want)
-    rows = [(0, t) for t in sample_positions(L, 1024, 1)]
+    rows = [(0, t) for t in sample_positions(L, 4096, 1)]
     check_rows(ref, job, rows, kidx, kv=lazy_kv(job.seed, L // BLK))
 
 
-def test_prefill_128k_sampled(ref):
+def whole_query_blocks(L, n):
+    """n query blocks (128 queries each) spread evenly over [0, L/128), first
+    and last included."""
+    nb = L // BLK
+    return sorted({round(k * (nb - 1) / (n - 1)) for k in range(n)})
+
+
+def test_prefill_128k_whole_query_blocks_and_sample(ref):
+    # Selections: every row of 64 whole query blocks spread evenly over the
+    # 131072 queries (8192 queries x 8 groups), plus the sampled rows below.
+    # A whole query block is 8 row tiles of the tensor-core scan, so every one
+    # of the 128 row positions of a tile (16 queries x 8 groups) is checked,
+    # for local blocks from 0 to 1023 (odd and even candidate counts, i.e.
+    # both halves of the last key-block pair), in tiles that the heaviest-
+    # first item order hands to CTAs early and late.  Attention: >= 4096
+    # sampled positions including the special ones.
     job = run_job("prefill_128k")
     L = job.L
     kidx = {0: syn.kidx_seq(job.seed, 0, L, DI)}
+    d = ref.dims(H, G, D, DI)
+    sel_gpu = job.sel.cpu().numpy()
+    for qb in whole_query_blocks(L, 64):
+        t0 = qb * BLK
+        q_idx = syn.qidx_rows(job.seed, 0, t0, t0 + BLK, G, DI)[None]
+        want = ref.index_topk(d, q_idx, kidx[0][None], t0, L, L // BLK)
+        assert np.array_equal(sel_gpu[0, t0:t0 + BLK], want[0]), qb
     rows = [(0, t) for t in sample_positions(L, 4096, 2)]
     check_rows(ref, job, rows, kidx, kv=lazy_kv(job.seed, L // BLK))
 
@@ -130,3 +153,48 @@ def test_prefill_1m_chunked_sampled(ref):
     edges = [c * 8192 + o for c in (1, 64, 127) for o in (-1, 0, 1)]
     rows = [(0, t) for t in sorted(set(sample_positions(L, 256, 4)) | set(edges))]
     check_rows(ref, job, rows, kidx, kv=lazy_kv(job.seed, L // BLK))
+
+
+def test_index_scan_row_tiles_beyond_2_17(ref):
+    # One prefill call with T*G > 2^24 (query, group) rows: the tensor-core
+    # scan's row tiles (128 rows each) then number more than 2^17.  Only the
+    # index step runs (steps 1-3), so no Q/K/V of this length is made.  Rows
+    # on both sides of tile 2^17 (query 2^21 at G = 8) are checked.
+    import torch
+    import block_sparse_attention_04_gb300 as msa
+    import msa_synth.device as sd
+    Gt, Dit = 8, 64
+    T = (1 << 21) + 700
+    nb = (T + BLK - 1) // BLK
+    seed = syn.BASE_SEED + 11
+    k_idx = torch.empty((1, nb * BLK, Dit), dtype=torch.int16, device="cuda")
+    sd.fill("grid", k_idx[0], seed, syn.TID_KIDX, 0)
+    sd.plant_needles(k_idx[0], T, Dit, seed, 0)
+    q_idx = torch.empty((1, T, Gt, Dit), dtype=torch.int16, device="cuda")
+    sd.fill("grid", q_idx[0], seed, syn.TID_QIDX, 0, 0)
+    p = msa.params(1, T, Gt, Gt, 64, Dit, nb, kernels="tensorcore")
+    ws = msa.workspace(p)
+    sel = torch.full((1, T, Gt, 16), -7, dtype=torch.int32, device="cuda")
+    msa.msa_index_topk(p, q_idx, k_idx, [0], [T], sel, ws)
+    msa.msa_workspace_status(ws)
+    torch.cuda.synchronize()
+    del ws, q_idx, k_idx
+    edge = 1 << 21          # first query of row tile 2^17
+    rng = np.random.default_rng(5)
+    ts = {edge - 17, edge - 16, edge - 1, edge, edge + 1, edge + 15, edge + 16, T - 1, T - 2,
+          300000}
+    ts |= {int(x) for x in rng.integers(edge, T, size=12)}
+    ts = sorted(ts)
+    got = sel[0, ts].cpu().numpy()
+    del sel
+    torch.cuda.empty_cache()
+    assert np.all(got != -7), "rows left unwritten"
+    kidx = syn.kidx_seq(seed, 0, T, Dit)
+    d = ref.dims(Gt, Gt, 64, Dit)
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+    with ThreadPoolExecutor(os.cpu_count() or 4) as pool:
+        want = list(pool.map(
+            lambda t: ref.select(d, t, syn.qidx_rows(seed, 0, t, t + 1, Gt, Dit)[0], kidx), ts))
+    for k, t in enumerate(ts):
+        assert np.array_equal(got[k], want[k]), (t, got[k].tolist(), want[k].tolist())

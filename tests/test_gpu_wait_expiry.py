@@ -1,0 +1,76 @@
+"""Failure path of the tensor-core kernels: a pipeline wait that runs out.
+
+Every wait between the warps of the tcgen05 index scan and of the KV-outer
+attention is bounded.  A test-only poll cap (msa_debug_set_wait_polls) makes
+those waits give up after one unsuccessful poll, so that a correct kernel on a
+healthy GPU meets the expiry path: it must record MSA_ERR_TIMEOUT in the
+workspace, drain the copies and MMAs it already issued, free its tensor memory
+and exit, leaving the CUDA context usable.  The very next call on the same
+workspace, with the cap removed, must then be bit-exact against the oracle.
+No GPU fault or hang is involved: the waits that run out are on work that
+would have completed a moment later.
+"""
+import numpy as np
+import pytest
+
+from tests.helpers import Workload, assert_close, assert_sel_equal, bf16_to_f64
+
+pytestmark = pytest.mark.gpu
+
+TIMEOUT = -5
+
+
+@pytest.fixture(scope="module")
+def msa():
+    import torch
+    assert torch.cuda.is_available()
+    import block_sparse_attention_04_gb300 as m
+    m.load()
+    return m
+
+
+def _status(msa, ws):
+    try:
+        msa.msa_workspace_status(ws)
+        return 0
+    except msa.MsaError as e:
+        return e.status
+
+
+def test_pipeline_wait_expiry_is_reported_then_next_call_is_exact(msa, ref):
+    import torch
+    wl = Workload(B=1, T=3000, H=48, G=8, D=128, Di=64, ctx=[6000], q_start=[3000])
+    want_sel, want_out = wl.oracle(ref)
+    dev = wl.device()
+    p = wl.params(msa, "tensorcore")
+    ws = msa.workspace(p)
+    sel = torch.full((1, wl.T, wl.G, 16), -7, dtype=torch.int32, device="cuda")
+    out = torch.zeros((1, wl.T, wl.H, wl.D), dtype=torch.int16, device="cuda")
+    ref_sel = torch.from_numpy(want_sel).cuda()
+
+    seen = {"index": [], "attn": []}
+    try:
+        msa.msa_debug_set_wait_polls(1)
+        for _ in range(3):
+            msa.msa_index_topk(p, dev["q_idx"], dev["k_idx"], wl.q_start, wl.kv_len, sel, ws)
+            seen["index"].append(_status(msa, ws))
+            msa.msa_sparse_attn(p, dev["q"], dev["k"], dev["v"], ref_sel, wl.q_start, wl.kv_len,
+                                out, ws)
+            seen["attn"].append(_status(msa, ws))
+    finally:
+        msa.msa_debug_set_wait_polls(0)
+    torch.cuda.synchronize()          # the context is still usable
+    for k, v in seen.items():
+        assert set(v) <= {0, TIMEOUT}, (k, v)
+        assert TIMEOUT in v, ("no wait ran out", k, v)
+
+    # the next calls on the same workspace: the status word is reset and the
+    # results are exact again
+    sel.fill_(-7)
+    out.fill_(0x7FC0)
+    msa.msa_index_topk(p, dev["q_idx"], dev["k_idx"], wl.q_start, wl.kv_len, sel, ws)
+    assert _status(msa, ws) == 0
+    msa.msa_sparse_attn(p, dev["q"], dev["k"], dev["v"], sel, wl.q_start, wl.kv_len, out, ws)
+    assert _status(msa, ws) == 0
+    assert_sel_equal(sel.cpu().numpy(), want_sel)
+    assert_close(bf16_to_f64(out.cpu().numpy()), want_out)
