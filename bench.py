@@ -46,7 +46,9 @@ WORKLOADS = {
                                   only_last=True),
 }
 DEFAULT_WORKLOAD = "prefill_1m"
-DEFAULT_SECONDARY = "decode_256k"
+# measured in the same run and nested in the default line, under these keys
+DEFAULT_SECONDARY = ("prefill_128k", "decode_256k")
+NESTED_KEY = {"prefill_128k": "prefill_128k", "decode_256k": "decode"}
 
 
 # ------------------------------------------------------------ algorithmic work --
@@ -271,7 +273,54 @@ def time_job(job, steps, warmup, world):
     return max_over_ranks(total_ms, world), idx_ms, att_ms, launches, ck
 
 
-def time_e2e(job, steps, world):
+class HostBuffers:
+    """Page-locked host tensors for the e2e leg.
+
+    kind "thp": anonymous memory advised onto transparent huge pages (the
+    host's PMD size), aligned to that size, then page-locked with
+    cudaHostRegister, so that a copy walks few, large physical runs; kind
+    "torch": torch's pinned allocator (cudaHostAlloc)."""
+
+    def __init__(self, kind):
+        self.kind, self.maps, self.regs = kind, [], []
+        self.huge = 2 << 20
+        try:
+            with open("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size") as f:
+                self.huge = int(f.read())
+        except (OSError, ValueError):
+            pass
+
+    def empty(self, shape, dtype):
+        import mmap
+        import torch
+        if self.kind == "torch":
+            return torch.empty(shape, dtype=dtype, pin_memory=True)
+        item = torch.empty((), dtype=dtype).element_size()
+        n = int(np.prod(shape)) * item
+        span = (n + 2 * self.huge - 1) // self.huge * self.huge
+        m = mmap.mmap(-1, span, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        base = np.frombuffer(m, dtype=np.uint8)
+        off = (-base.ctypes.data) % self.huge
+        try:
+            m.madvise(mmap.MADV_HUGEPAGE, off, span - off)
+        except (AttributeError, OSError, ValueError):
+            pass
+        t = torch.frombuffer(m, dtype=dtype, count=n // item, offset=off).view(shape)
+        rc = torch.cuda.cudart().cudaHostRegister(t.data_ptr(), n, 0)
+        if int(rc) != 0:
+            raise RuntimeError("cudaHostRegister failed (%s)" % rc)
+        self.maps.append((m, base))
+        self.regs.append(t.data_ptr())
+        return t
+
+    def release(self):
+        import torch
+        for ptr in self.regs:
+            torch.cuda.cudart().cudaHostUnregister(ptr)
+        self.regs = []
+
+
+def time_e2e(job, steps, world, host_alloc="thp"):
     """Same step through the C ABI with host buffers: pinned H2D of the step's
     inputs and D2H of its outputs inside the timed region."""
     import torch
@@ -279,11 +328,12 @@ def time_e2e(job, steps, world):
         names = ["q_idx", "q"]      # the caches stay resident between decode steps
     else:
         names = ["q_idx", "k_idx", "q", "k", "v"]
-    host = {n: torch.empty(job.dev[n].shape, dtype=torch.int16, pin_memory=True) for n in names}
+    bufs = HostBuffers(host_alloc)
+    host = {n: bufs.empty(job.dev[n].shape, torch.int16) for n in names}
     for n in names:
         host[n].copy_(job.dev[n])
-    sel_h = torch.empty(job.sel.shape, dtype=torch.int32, pin_memory=True)
-    out_h = torch.empty(job.out.shape, dtype=torch.int16, pin_memory=True)
+    sel_h = bufs.empty(job.sel.shape, torch.int32)
+    out_h = bufs.empty(job.out.shape, torch.int16)
     h2d = sum(host[n].numel() * 2 for n in names)
     d2h = sel_h.numel() * 4 + out_h.numel() * 2
     t0 = torch.cuda.Event(enable_timing=True)
@@ -340,6 +390,8 @@ def time_e2e(job, steps, world):
     t1.record()
     torch.cuda.synchronize()
     ms = max_over_ranks(t0.elapsed_time(t1), world) / steps
+    del host, sel_h, out_h
+    bufs.release()
     return ms, h2d, d2h
 
 
@@ -437,12 +489,39 @@ def reference_arm(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the index
-# scan's kernels per msa_index_topk call, averaged over the calls of one step,
-# from a single-pass ncu capture of the same workload (the index scan traffic
-# summary under profiles/).  These are measurements of the kernels as they
-# were then: reset an entry to None whenever those kernels change.
-INDEX_TRAFFIC = {"prefill_1m": 1134451984, "decode_256k": 2150751488}
+# DRAM traffic of the dominant kernel comes from a recorded ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum of one launch on a small case,
+# scaled to this workload's launches by the algorithmic work), stored with a
+# hash of the kernel sources it was taken on.  When those sources change, the
+# figure no longer describes the kernel and `traffic` is reported as null.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+KERNEL_SOURCES = {
+    "index_tc": ["msa_index_tc.cu", "msa_device.cuh", "msa_internal.h"],
+    "index_stream": ["msa_stream.cu", "msa_device.cuh", "msa_internal.h"],
+}
+
+
+def kernel_sources_sha(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "block_sparse_attention_04_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, units_per_launch):
+    """DRAM bytes per launch of `kernel` for a launch processing units_per_launch
+    algorithmic units (flops or bytes), or None if no capture matches the
+    current sources."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)[kernel]
+    except (OSError, ValueError, KeyError):
+        return None
+    if rec.get("sources_sha") != kernel_sources_sha(kernel):
+        return None
+    return rec["dram_bytes"] * units_per_launch / rec["units"]
 
 
 def measure(name, args, world, rank):
@@ -460,7 +539,8 @@ def measure(name, args, world, rank):
         roof = {"bound": "hbm",
                 "kernel": "index scan (msa_index_topk: index_stream + topk_merge)",
                 "achieved": kidx_b / (idx_ms / 1000.0) / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "traffic": INDEX_TRAFFIC.get(name), "peak_kind": peak_kind,
+                "unit": "GB/s", "traffic": recorded_traffic("index_stream", kidx_b),
+                "peak_kind": peak_kind,
                 "bytes_per_launch": kidx_b}
         roof["frac"] = roof["achieved"] / roof["peak"]
         whole = {"bytes_per_step": kidx_b + rest_b,
@@ -475,7 +555,7 @@ def measure(name, args, world, rank):
         roof = {"bound": "tensor",
                 "kernel": "index scan (msa_index_topk: index_tc + topk_merge)",
                 "achieved": fi / (idx_ms / 1000.0) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
-                "traffic": INDEX_TRAFFIC.get(name),
+                "traffic": recorded_traffic("index_tc", fi / len(job.calls)),
                 "peak_kind": peak_kind + (" sustained" if sustained else " burst"),
                 "flops_per_step": fi, "launches_per_step": len(job.calls)}
         roof["frac"] = roof["achieved"] / roof["peak"]
@@ -483,7 +563,7 @@ def measure(name, args, world, rank):
                  "achieved_tflops": (fi + fa) / (ms / 1000.0) / 1e12,
                  "attn_achieved_tflops": fa / (att_ms / 1000.0) / 1e12}
         whole["frac_of_bf16_peak"] = whole["achieved_tflops"] / peak_tf
-    e2e_ms, h2d, d2h = time_e2e(job, max(1, min(args.steps, 3)), world)
+    e2e_ms, h2d, d2h = time_e2e(job, max(1, min(args.steps, 3)), world, args.host_alloc)
     cfg = {"workload": name, "batch": job.B, "ctx": job.L, "calls_per_step": len(job.calls),
            "queries_per_call": job.calls[0]["T"], "heads": H, "kv_heads": G, "head_dim": D,
            "index_dim": DI, "block": BLK, "topk": 16, "l2": "inputs larger than L2 (no flush)"}
@@ -498,7 +578,9 @@ def measure(name, args, world, rank):
     return {"value": tokens / (ms / 1000.0), "ms_per_step": ms, "config": cfg, "roofline": roof,
             "step": whole, "kernels_ms": {"index_topk": idx_ms, "sparse_attn": att_ms},
             "e2e": {"value": tokens / (e2e_ms / 1000.0), "unit": "tokens/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "host_buffers": {"thp": "page-locked transparent huge pages",
+                                     "torch": "torch pinned allocator"}[args.host_alloc]},
             "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu}
 
 
@@ -516,10 +598,12 @@ def gpu_arm(args, world, rank):
     for k in ("config", "roofline", "step", "kernels_ms", "e2e", "gpu_launches", "clocks",
               "cpu_baseline"):
         line[k] = r[k]
-    if args.secondary and args.secondary != args.workload:
-        s = measure(args.secondary, args, world, rank)
-        line[WORKLOADS[args.secondary]["kind"]] = {
-            "workload": args.secondary, "value": s["value"], "unit": "tokens/s",
+    for sec in args.secondary:
+        if sec == args.workload:
+            continue
+        s = measure(sec, args, world, rank)
+        line[NESTED_KEY.get(sec, sec)] = {
+            "workload": sec, "value": s["value"], "unit": "tokens/s",
             "ms_per_step": s["ms_per_step"], "config": s["config"], "roofline": s["roofline"],
             "step": s["step"], "kernels_ms": s["kernels_ms"], "e2e": s["e2e"],
             "gpu_launches": s["gpu_launches"], "clocks": s["clocks"],
@@ -538,14 +622,22 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=None,
                     help="rows of the bounded oracle sample per reference step")
     ap.add_argument("--secondary", default=None,
-                    help="a second workload reported in the same line (default: decode_256k "
-                         "when the workload is the default one; 'none' to skip)")
+                    help="comma-separated workloads reported in the same line (default: "
+                         "prefill_128k,decode_256k when the workload is the default one; "
+                         "'none' to skip)")
+    ap.add_argument("--host-alloc", choices=["thp", "torch"], default="thp",
+                    help="host buffers of the e2e leg: page-locked transparent huge pages "
+                         "(default) or torch's pinned allocator")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     args = ap.parse_args()
     if args.secondary is None:
-        args.secondary = DEFAULT_SECONDARY if args.workload == DEFAULT_WORKLOAD else "none"
-    if args.secondary == "none":
-        args.secondary = None
+        args.secondary = ",".join(DEFAULT_SECONDARY) if args.workload == DEFAULT_WORKLOAD \
+            else "none"
+    args.secondary = [] if args.secondary == "none" else \
+        [w for w in args.secondary.split(",") if w]
+    for w in args.secondary:
+        if w not in WORKLOADS:
+            ap.error("unknown workload %r" % w)
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
         rank = int(os.environ.get("RANK", "0"))
