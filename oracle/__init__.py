@@ -50,11 +50,13 @@ def _bind(path):
     L.msa_ref_select.argtypes = [ctypes.POINTER(Dims), i64, P, P, P, P]
     L.msa_ref_attend.argtypes = [ctypes.POINTER(Dims), i64, P, P, P, P, P]
     L.msa_ref_dense.argtypes = [ctypes.POINTER(Dims), i64, P, P, P, P]
+    L.msa_ref_quality.argtypes = [ctypes.POINTER(Dims), i64, P, P, P, P, P, P, P, P]
     L.msa_ref_index_topk.argtypes = [ctypes.POINTER(Dims), ci, ci, ci, P, P, P, P, P, ci]
     L.msa_ref_sparse_attn.argtypes = [ctypes.POINTER(Dims), ci, ci, ci, P, P, P, P, P, P,
                                       P, ci]
     L.msa_ref_dense_attn.argtypes = [ctypes.POINTER(Dims), ci, ci, ci, P, P, P, P, P, P, ci]
-    for f in ("msa_ref_select", "msa_ref_attend", "msa_ref_dense", "msa_ref_index_topk",
+    for f in ("msa_ref_select", "msa_ref_attend", "msa_ref_dense", "msa_ref_quality",
+              "msa_ref_index_topk",
               "msa_ref_sparse_attn", "msa_ref_dense_attn"):
         getattr(L, f).restype = ctypes.c_int
     return L
@@ -136,6 +138,26 @@ def dense(d, t, q_t, k_seq, v_seq):
     _check(lib().msa_ref_dense(ctypes.byref(d), t, _p(q_t), _p(k_seq), _p(v_seq), _p(out)),
            "dense")
     return out
+
+
+def quality(d, t, q_t, k_seq, sel_t, want_mass=False):
+    """Selection quality of one query (see msa_ref.h): q_t [H][D], k_seq
+    [nblocks][block][G][D], sel_t [G][topk] -> dict(coverage [H],
+    best_coverage [H], dense_sel [G][topk], hits [G], mass [G][lb+1] if asked)."""
+    q_t, k_seq = _u16(q_t), _u16(k_seq)
+    sel_t = np.ascontiguousarray(sel_t, np.int32)
+    cov = np.empty(d.H, np.float64)
+    best = np.empty(d.H, np.float64)
+    ds = np.empty((d.G, d.topk), np.int32)
+    hits = np.empty(d.G, np.int32)
+    mass = np.empty((d.G, t // d.block + 1), np.float64) if want_mass else None
+    _check(lib().msa_ref_quality(ctypes.byref(d), t, _p(q_t), _p(k_seq), _p(sel_t), _p(cov),
+                                 _p(best), _p(ds), _p(hits), _p(mass) if want_mass else None),
+           "quality")
+    r = dict(coverage=cov, best_coverage=best, dense_sel=ds, hits=hits)
+    if want_mass:
+        r["mass"] = mass
+    return r
 
 
 def _pos(B, q_start, kv_len):

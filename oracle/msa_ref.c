@@ -181,6 +181,91 @@ int msa_ref_dense(const msa_ref_dims *p, int64_t t, const uint16_t *q_t, const u
   return attend_tokens(p, t, q_t, k, v, NULL, 1, out_t);
 }
 
+/* Attention mass per block and head under the full causal softmax, then the
+ * ideal selection under the MSA rule, and how much of the mass the given and
+ * the ideal selections hold.  Double throughout. */
+int msa_ref_quality(const msa_ref_dims *p, int64_t t, const uint16_t *q_t, const uint16_t *k,
+                    const int32_t *sel_t, double *coverage, double *best_coverage,
+                    int32_t *dense_sel, int32_t *hits, double *mass) {
+  if (!dims_ok(p) || t < 0 || !q_t || !k || !sel_t || !coverage || !best_coverage ||
+      !dense_sel || !hits)
+    return -1;
+  const int hpg = p->H / p->G;
+  const size_t row = (size_t)p->G * p->D;
+  const int64_t lb = t / p->block, nblk = lb + 1;
+  double *z = (double *)malloc((size_t)(t + 1) * sizeof(double));
+  double *A = (double *)malloc((size_t)hpg * nblk * sizeof(double)); /* [hh][b] */
+  double *P = (double *)malloc((size_t)nblk * sizeof(double));
+  cand_t *cand = (cand_t *)malloc((size_t)(lb > 0 ? lb : 1) * sizeof(cand_t));
+  if (!z || !A || !P || !cand) {
+    free(z); free(A); free(P); free(cand);
+    return -1;
+  }
+  for (int g = 0; g < p->G; ++g) {
+    for (int64_t b = 0; b < nblk; ++b) P[b] = 0.0;
+    for (int hh = 0; hh < hpg; ++hh) {
+      const uint16_t *qh = q_t + (size_t)(g * hpg + hh) * p->D;
+      /* the full causal softmax of head h: every token 0..t */
+      double m = -INFINITY;
+      for (int64_t i = 0; i <= t; ++i) {
+        const uint16_t *kr = k + (size_t)i * row + (size_t)g * p->D;
+        double s = 0.0;
+        for (int d = 0; d < p->D; ++d) s += bf16_to_double(qh[d]) * bf16_to_double(kr[d]);
+        z[i] = s * p->scale;
+        if (z[i] > m) m = z[i];
+      }
+      double Z = 0.0;
+      for (int64_t i = 0; i <= t; ++i) {
+        z[i] = exp(z[i] - m);
+        Z += z[i];
+      }
+      double *Ah = A + (size_t)hh * nblk;
+      for (int64_t b = 0; b < nblk; ++b) Ah[b] = 0.0;
+      for (int64_t i = 0; i <= t; ++i) Ah[i / p->block] += z[i] / Z;
+      for (int64_t b = 0; b < nblk; ++b) P[b] += Ah[b] / hpg;
+    }
+    if (mass)
+      for (int64_t b = 0; b < nblk; ++b) mass[(size_t)g * nblk + b] = P[b];
+    /* the ideal selection: local block forced, then the best candidates by
+     * group-averaged mass (same ranking rule as the index branch) */
+    for (int64_t b = 0; b < lb; ++b) {
+      cand[b].score = P[b];
+      cand[b].blk = (int32_t)b;
+    }
+    qsort(cand, (size_t)lb, sizeof(cand_t), cand_cmp);
+    const int64_t nsel = lb + 1 < p->topk ? lb + 1 : p->topk;
+    int32_t *ds = dense_sel + (size_t)g * p->topk;
+    ds[0] = (int32_t)lb;
+    for (int64_t i = 1; i < nsel; ++i) ds[i] = cand[i - 1].blk;
+    qsort(ds, (size_t)nsel, sizeof(int32_t), int_cmp);
+    for (int64_t i = nsel; i < p->topk; ++i) ds[i] = -1;
+    /* the given selection as a set of distinct valid ids */
+    const int32_t *s = sel_t + (size_t)g * p->topk;
+    int32_t given[64];
+    int ng = 0;
+    for (int j = 0; j < p->topk && j < 64; ++j) {
+      if (s[j] < 0 || s[j] > lb) continue;
+      int dup = 0;
+      for (int u = 0; u < ng; ++u) dup |= given[u] == s[j];
+      if (!dup) given[ng++] = s[j];
+    }
+    int h = 0;
+    for (int u = 0; u < ng; ++u)
+      for (int64_t i = 0; i < nsel; ++i) h += given[u] == ds[i];
+    hits[g] = h;
+    for (int hh = 0; hh < hpg; ++hh) {
+      const double *Ah = A + (size_t)hh * nblk;
+      double c = 0.0, cb = 0.0;
+      for (int u = 0; u < ng; ++u) c += Ah[given[u]];
+      for (int64_t i = 0; i < nsel; ++i) cb += Ah[ds[i]];
+      coverage[g * hpg + hh] = c;
+      best_coverage[g * hpg + hh] = cb;
+    }
+  }
+  free(z); free(A); free(P); free(cand);
+  return 0;
+}
+
 static int batch_ok(const msa_ref_dims *p, int B, int T, int max_blocks, const int32_t *q_start,
                     const int32_t *kv_len) {
   if (!dims_ok(p) || B < 0 || T < 0 || max_blocks < 0 || !q_start || !kv_len) return 0;

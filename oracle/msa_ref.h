@@ -57,6 +57,25 @@ int msa_ref_attend(const msa_ref_dims *p, int64_t t, const uint16_t *q_t,
 int msa_ref_dense(const msa_ref_dims *p, int64_t t, const uint16_t *q_t,
                   const uint16_t *k, const uint16_t *v, double *out_t);
 
+/* Selection quality of one query (the evaluation the same section asks for:
+ * how much of the attention the selected blocks recall).  For every head h
+ * of every group g, with alpha_h the full causal softmax over all tokens
+ * <= t (no selection) and A_h(b) = sum of alpha_h over the tokens of block b:
+ *   coverage[h]      = sum of A_h(b) over the distinct valid ids b in sel_t[g]
+ *   best_coverage[h] = sum of A_h(b) over b in dense_sel[g]
+ *   dense_sel[g]     = the selection a perfect indexer would make under the
+ *                      same rule: the local block lb plus the top
+ *                      min(16, lb+1) - 1 blocks b < lb by the group-averaged
+ *                      mass P_g(b) = mean over the group's heads of A_h(b)
+ *                      (ties to the lower id), ascending, -1 padded
+ *   hits[g]          = |sel_t[g] intersected with dense_sel[g]|
+ * Selection recall is hits[g] / min(16, lb+1).  mass (optional, may be NULL):
+ * [G][lb+1] receives P_g(b).  sel_t [G][topk]; q_t [H][D]; k as in attend. */
+int msa_ref_quality(const msa_ref_dims *p, int64_t t, const uint16_t *q_t,
+                    const uint16_t *k, const int32_t *sel_t, double *coverage,
+                    double *best_coverage, int32_t *dense_sel, int32_t *hits,
+                    double *mass);
+
 /* Batched forms over the library layouts, OpenMP over queries when
  * nthreads > 1.  kv_len[b] bounds the causal context: q_start[b] + T <=
  * kv_len[b] <= max_blocks*block. */

@@ -11,6 +11,7 @@ import pytest
 
 import oracle
 from tests import test_oracle as pins
+from tests import test_oracle_quality as qpins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "msa_ref.c")
 
@@ -23,12 +24,13 @@ MUTANTS = {
     # sum pooling instead of max pooling
     "sum_pool": ("if (s > best) best = s;", "best = (best == -INFINITY ? 0.0 : best) + s;"),
     # plain top-16 of the candidates: the local block is not forced in
-    "local_not_forced": ("s[0] = (int32_t)lb;",
-                         "s[0] = lb >= p->topk ? cand[p->topk - 1].blk : (int32_t)lb;"),
+    "local_not_forced": ("\n    s[0] = (int32_t)lb;",
+                         "\n    s[0] = lb >= p->topk ? cand[p->topk - 1].blk : (int32_t)lb;"),
     # causal clip of the local block dropped
     "no_causal_clip": ("if (tok > t) continue;", "(void)0;"),
     # softmax scale dropped
-    "no_scale": ("z[i] = s * p->scale;", "z[i] = s;"),
+    "no_scale": ("z[i] = s * p->scale;\n      }\n      softmax_combine",
+                 "z[i] = s;\n      }\n      softmax_combine"),
     # wrong KV head for a query head (reversed group order)
     "wrong_kv_head": ("krow[n] = k + (size_t)tok * row + (size_t)g * p->D;\n          vrow",
                       "krow[n] = k + (size_t)tok * row + (size_t)(p->G - 1 - g) * p->D;\n          vrow"),
@@ -38,6 +40,22 @@ MUTANTS = {
     # softmax normaliser off by one
     "bad_normaliser": ("for (int d = 0; d < D; ++d) out[d] /= l;",
                        "for (int d = 0; d < D; ++d) out[d] /= (l + 1.0);"),
+    # selection quality: block masses not normalised by the softmax sum
+    "quality_unnormalised_mass": ("Ah[i / p->block] += z[i] / Z;", "Ah[i / p->block] += z[i];"),
+    # selection quality: ideal selection ranked by the group's last head only
+    "quality_last_head_only": ("P[b] += Ah[b] / hpg;", "P[b] = Ah[b];"),
+    # selection quality: local block not forced into the ideal selection
+    "quality_local_not_forced": ("ds[0] = (int32_t)lb;",
+                                 "ds[0] = lb >= p->topk ? cand[p->topk - 1].blk : (int32_t)lb;"),
+    # selection quality: every head scored with its group's first head
+    "quality_wrong_head": ("const uint16_t *qh = q_t + (size_t)(g * hpg + hh) * p->D;\n      /*",
+                           "const uint16_t *qh = q_t + (size_t)(g * hpg) * p->D;\n      /*"),
+    # selection quality: softmax scale dropped
+    "quality_no_scale": ("z[i] = s * p->scale;\n        if (z[i] > m)",
+                         "z[i] = s;\n        if (z[i] > m)"),
+    # selection quality: the full softmax stops at the local block's start
+    "quality_no_local_tokens": ("      for (int64_t i = 0; i <= t; ++i) {\n        const uint16_t *kr",
+                                "      for (int64_t i = 0; i < lb * p->block; ++i) {\n        const uint16_t *kr"),
 }
 
 PINS = [
@@ -48,6 +66,10 @@ PINS = [
     pins.test_short_context_equals_full_causal_attention,
     pins.test_sparse_equals_masked_sdpa,
     pins.test_closed_forms,
+    qpins.test_quality_block_masses_and_ideal_selection_match_sdpa,
+    qpins.test_quality_short_context_recalls_everything,
+    qpins.test_quality_dominant_key_closed_form,
+    qpins.test_quality_ideal_selection_dominates_the_index_selection,
 ]
 
 
