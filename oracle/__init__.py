@@ -51,12 +51,15 @@ def _bind(path):
     L.msa_ref_attend.argtypes = [ctypes.POINTER(Dims), i64, P, P, P, P, P]
     L.msa_ref_dense.argtypes = [ctypes.POINTER(Dims), i64, P, P, P, P]
     L.msa_ref_quality.argtypes = [ctypes.POINTER(Dims), i64, P, P, P, P, P, P, P, P]
+    L.msa_ref_index_kl.argtypes = [ctypes.POINTER(Dims), i64, P, P, P, P, P, P, P, P]
+    L.msa_ref_index_kl_batch.argtypes = [ctypes.POINTER(Dims), ci, ci, ci, P, P, P, P, P, P, P,
+                                         P, P, P, ci]
     L.msa_ref_index_topk.argtypes = [ctypes.POINTER(Dims), ci, ci, ci, P, P, P, P, P, ci]
     L.msa_ref_sparse_attn.argtypes = [ctypes.POINTER(Dims), ci, ci, ci, P, P, P, P, P, P,
                                       P, ci]
     L.msa_ref_dense_attn.argtypes = [ctypes.POINTER(Dims), ci, ci, ci, P, P, P, P, P, P, ci]
     for f in ("msa_ref_select", "msa_ref_attend", "msa_ref_dense", "msa_ref_quality",
-              "msa_ref_index_topk",
+              "msa_ref_index_kl", "msa_ref_index_kl_batch", "msa_ref_index_topk",
               "msa_ref_sparse_attn", "msa_ref_dense_attn"):
         getattr(L, f).restype = ctypes.c_int
     return L
@@ -158,6 +161,37 @@ def quality(d, t, q_t, k_seq, sel_t, want_mass=False):
     if want_mass:
         r["mass"] = mass
     return r
+
+
+def index_kl(d, t, q_idx_t, k_idx_seq, q_t, k_seq, sel_t, dk_idx=None):
+    """One query's KL(P||Q) per group and its gradient (see msa_ref.h):
+    returns (kl [G], dq_idx [G][Di]); dk_idx [>= t+1][Di] float64 is
+    accumulated into when given."""
+    q_idx_t, k_idx_seq, q_t, k_seq = _u16(q_idx_t), _u16(k_idx_seq), _u16(q_t), _u16(k_seq)
+    sel_t = np.ascontiguousarray(sel_t, np.int32)
+    kl = np.empty(d.G, np.float64)
+    dq = np.empty((d.G, d.Di), np.float64)
+    if dk_idx is None:
+        dk_idx = np.zeros((t + 1, d.Di), np.float64)
+    assert dk_idx.dtype == np.float64 and dk_idx.flags.c_contiguous and dk_idx.shape[0] > t
+    _check(lib().msa_ref_index_kl(ctypes.byref(d), t, _p(q_idx_t), _p(k_idx_seq), _p(q_t),
+                                  _p(k_seq), _p(sel_t), _p(kl), _p(dq), _p(dk_idx)), "index_kl")
+    return kl, dq
+
+
+def index_kl_batch(d, q_idx, k_idx, q, k, sel, q_start, kv_len, max_blocks, nthreads=None):
+    """kl [B][T][G], dq_idx [B][T][G][Di], dk_idx [B][max_blocks*block][Di]."""
+    q_idx, k_idx, q, k = _u16(q_idx), _u16(k_idx), _u16(q), _u16(k)
+    sel = np.ascontiguousarray(sel, np.int32)
+    B, T = q.shape[0], q.shape[1]
+    qs, kl_ = _pos(B, q_start, kv_len)
+    kl = np.empty((B, T, d.G), np.float64)
+    dq = np.empty((B, T, d.G, d.Di), np.float64)
+    dk = np.zeros((B, max_blocks * d.block, d.Di), np.float64)
+    _check(lib().msa_ref_index_kl_batch(ctypes.byref(d), B, T, max_blocks, _p(q_idx), _p(k_idx),
+                                        _p(q), _p(k), _p(sel), _p(qs), _p(kl_), _p(kl), _p(dq),
+                                        _p(dk), nthreads or nthreads_default()), "index_kl_batch")
+    return kl, dq, dk
 
 
 def _pos(B, q_start, kv_len):

@@ -266,6 +266,105 @@ int msa_ref_quality(const msa_ref_dims *p, int64_t t, const uint16_t *q_t, const
   return 0;
 }
 
+/* The candidate blocks of one group: the distinct ids of s in [0, lb], in
+ * slot order. */
+static int candidates(const int32_t *s, int topk, int64_t lb, int32_t *out) {
+  int n = 0;
+  for (int j = 0; j < topk; ++j) {
+    if (s[j] < 0 || s[j] > lb) continue;
+    int dup = 0;
+    for (int u = 0; u < n; ++u) dup |= out[u] == s[j];
+    if (!dup) out[n++] = s[j];
+  }
+  return n;
+}
+
+int msa_ref_index_kl(const msa_ref_dims *p, int64_t t, const uint16_t *q_idx_t,
+                     const uint16_t *k_idx, const uint16_t *q_t, const uint16_t *k,
+                     const int32_t *sel_t, double *kl, double *dq_idx, double *dk_idx) {
+  if (!dims_ok(p) || t < 0 || !q_idx_t || !k_idx || !q_t || !k || !sel_t || !kl || !dq_idx ||
+      !dk_idx || p->topk > 64)
+    return -1;
+  const int hpg = p->H / p->G;
+  const size_t row = (size_t)p->G * p->D;
+  const int64_t lb = t / p->block;
+  double *z = (double *)malloc((size_t)p->topk * p->block * sizeof(double));
+  if (!z) return -1;
+  for (int g = 0; g < p->G; ++g) {
+    int32_t c[64];
+    const int n = candidates(sel_t + (size_t)g * p->topk, p->topk, lb, c);
+    double P[64], zi[64], Q[64];
+    int64_t arg[64];
+    for (int j = 0; j < n; ++j) P[j] = 0.0;
+    /* P: the main branch's softmax over the selected tokens, mass per block,
+     * averaged over the group's heads */
+    for (int hh = 0; hh < hpg; ++hh) {
+      const uint16_t *qh = q_t + (size_t)(g * hpg + hh) * p->D;
+      double m = -INFINITY;
+      int64_t ntok = 0;
+      for (int j = 0; j < n; ++j)
+        for (int64_t tok = (int64_t)c[j] * p->block; tok < ((int64_t)c[j] + 1) * p->block; ++tok) {
+          if (tok > t) continue;
+          const uint16_t *kr = k + (size_t)tok * row + (size_t)g * p->D;
+          double s = 0.0;
+          for (int d = 0; d < p->D; ++d) s += bf16_to_double(qh[d]) * bf16_to_double(kr[d]);
+          z[ntok] = s * p->scale;
+          if (z[ntok] > m) m = z[ntok];
+          ++ntok;
+        }
+      double Z = 0.0;
+      for (int64_t i = 0; i < ntok; ++i) Z += exp(z[i] - m);
+      int64_t i = 0;
+      for (int j = 0; j < n; ++j)
+        for (int64_t tok = (int64_t)c[j] * p->block; tok < ((int64_t)c[j] + 1) * p->block; ++tok) {
+          if (tok > t) continue;
+          P[j] += exp(z[i++] - m) / Z / hpg;
+        }
+    }
+    /* Q: softmax of the pooled index scores of the same blocks */
+    const uint16_t *qi = q_idx_t + (size_t)g * p->Di;
+    double zmax = -INFINITY;
+    for (int j = 0; j < n; ++j) {
+      zi[j] = -INFINITY;
+      arg[j] = -1;
+      for (int64_t tok = (int64_t)c[j] * p->block; tok < ((int64_t)c[j] + 1) * p->block; ++tok) {
+        if (tok > t) continue;
+        const uint16_t *kr = k_idx + (size_t)tok * p->Di;
+        double s = 0.0;
+        for (int d = 0; d < p->Di; ++d) s += bf16_to_double(qi[d]) * bf16_to_double(kr[d]);
+        if (s > zi[j]) { /* strictly greater: the first maximal token wins */
+          zi[j] = s;
+          arg[j] = tok;
+        }
+      }
+      if (zi[j] > zmax) zmax = zi[j];
+    }
+    double sq = 0.0;
+    for (int j = 0; j < n; ++j) sq += exp(zi[j] - zmax);
+    double loss = 0.0;
+    for (int j = 0; j < n; ++j) {
+      Q[j] = exp(zi[j] - zmax) / sq;
+      if (P[j] > 0.0) loss += P[j] * (log(P[j]) - log(Q[j]));
+    }
+    kl[g] = loss;
+    /* gradient through the pooled scores to the maximal tokens */
+    double *dq = dq_idx + (size_t)g * p->Di;
+    for (int d = 0; d < p->Di; ++d) dq[d] = 0.0;
+    for (int j = 0; j < n; ++j) {
+      const double dz = Q[j] - P[j];
+      const uint16_t *kr = k_idx + (size_t)arg[j] * p->Di;
+      double *dk = dk_idx + (size_t)arg[j] * p->Di;
+      for (int d = 0; d < p->Di; ++d) {
+        dq[d] += dz * bf16_to_double(kr[d]);
+#pragma omp atomic
+        dk[d] += dz * bf16_to_double(qi[d]);
+      }
+    }
+  }
+  free(z);
+  return 0;
+}
+
 static int batch_ok(const msa_ref_dims *p, int B, int T, int max_blocks, const int32_t *q_start,
                     const int32_t *kv_len) {
   if (!dims_ok(p) || B < 0 || T < 0 || max_blocks < 0 || !q_start || !kv_len) return 0;
@@ -333,4 +432,32 @@ int msa_ref_dense_attn(const msa_ref_dims *p, int B, int T, int max_blocks, cons
                        const uint16_t *k, const uint16_t *v, const int32_t *q_start,
                        const int32_t *kv_len, double *out, int nthreads) {
   return batched_attn(p, B, T, max_blocks, q, k, v, NULL, q_start, kv_len, out, nthreads, 1);
+}
+
+int msa_ref_index_kl_batch(const msa_ref_dims *p, int B, int T, int max_blocks,
+                           const uint16_t *q_idx, const uint16_t *k_idx, const uint16_t *q,
+                           const uint16_t *k, const int32_t *sel, const int32_t *q_start,
+                           const int32_t *kv_len, double *kl, double *dq_idx, double *dk_idx,
+                           int nthreads) {
+  if (!batch_ok(p, B, T, max_blocks, q_start, kv_len) || !q_idx || !k_idx || !q || !k || !sel ||
+      !kl || !dq_idx || !dk_idx)
+    return -1;
+  const size_t cap = (size_t)max_blocks * p->block;
+  const size_t seq = cap * p->G * p->D;
+  int rc = 0;
+  const int64_t n = (int64_t)B * T;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
+  for (int64_t r = 0; r < n; ++r) {
+    const int b = (int)(r / T), i = (int)(r % T);
+    int e = msa_ref_index_kl(p, (int64_t)q_start[b] + i, q_idx + (size_t)r * p->G * p->Di,
+                             k_idx + (size_t)b * cap * p->Di, q + (size_t)r * p->H * p->D,
+                             k + (size_t)b * seq, sel + (size_t)r * p->G * p->topk,
+                             kl + (size_t)r * p->G, dq_idx + (size_t)r * p->G * p->Di,
+                             dk_idx + (size_t)b * cap * p->Di);
+    if (e) {
+#pragma omp atomic write
+      rc = e;
+    }
+  }
+  return rc;
 }

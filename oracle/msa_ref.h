@@ -76,6 +76,25 @@ int msa_ref_quality(const msa_ref_dims *p, int64_t t, const uint16_t *q_t,
                     double *best_coverage, int32_t *dense_sel, int32_t *hits,
                     double *mass);
 
+/* Training signal of the index branch for one query ("MiniMax 模型迭代与竞品
+ * 分析" section 2, the paragraph on how the indexer learns to select): over
+ * the candidate blocks C = the distinct valid ids of sel_t[g],
+ *   P_j  = mean over the group's heads of the main branch's softmax mass on
+ *          block j (the sparse softmax over the selected tokens <= t);
+ *          a target: no gradient flows into it
+ *   z_j  = the block's pooled index score, max over its tokens <= t of
+ *          <Q_idx[t,g], K_idx[tok]>, attained first at token a_j
+ *   Q_j  = exp(z_j) / sum over C of exp(z_c)
+ *   kl[g] = sum over C of P_j (ln P_j - ln Q_j)      (terms with P_j = 0 vanish)
+ * and its gradient: dz_j = Q_j - P_j, so
+ *   dq_idx[g][d]  = sum_j dz_j K_idx[a_j][d]              (written)
+ *   dk_idx[a_j][d] += dz_j Q_idx[t,g][d]                  (accumulated)
+ * q_idx_t [G][Di]; k_idx [>= t+1][Di]; q_t [H][D]; k as in attend; sel_t
+ * [G][topk]; kl [G]; dq_idx [G][Di]; dk_idx [>= t+1][Di] (double). */
+int msa_ref_index_kl(const msa_ref_dims *p, int64_t t, const uint16_t *q_idx_t,
+                     const uint16_t *k_idx, const uint16_t *q_t, const uint16_t *k,
+                     const int32_t *sel_t, double *kl, double *dq_idx, double *dk_idx);
+
 /* Batched forms over the library layouts, OpenMP over queries when
  * nthreads > 1.  kv_len[b] bounds the causal context: q_start[b] + T <=
  * kv_len[b] <= max_blocks*block. */
@@ -88,6 +107,14 @@ int msa_ref_sparse_attn(const msa_ref_dims *p, int B, int T, int max_blocks,
                         const uint16_t *q, const uint16_t *k, const uint16_t *v,
                         const int32_t *sel, const int32_t *q_start,
                         const int32_t *kv_len, double *out, int nthreads);
+
+/* msa_ref_index_kl for every query of a batch: kl [B][T][G], dq_idx
+ * [B][T][G][Di] written, dk_idx [B][max_blocks*block][Di] accumulated. */
+int msa_ref_index_kl_batch(const msa_ref_dims *p, int B, int T, int max_blocks,
+                           const uint16_t *q_idx, const uint16_t *k_idx,
+                           const uint16_t *q, const uint16_t *k, const int32_t *sel,
+                           const int32_t *q_start, const int32_t *kv_len, double *kl,
+                           double *dq_idx, double *dk_idx, int nthreads);
 
 int msa_ref_dense_attn(const msa_ref_dims *p, int B, int T, int max_blocks,
                        const uint16_t *q, const uint16_t *k, const uint16_t *v,

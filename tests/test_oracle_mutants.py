@@ -11,6 +11,7 @@ import pytest
 
 import oracle
 from tests import test_oracle as pins
+from tests import test_oracle_kl as klpins
 from tests import test_oracle_quality as qpins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "msa_ref.c")
@@ -27,7 +28,7 @@ MUTANTS = {
     "local_not_forced": ("\n    s[0] = (int32_t)lb;",
                          "\n    s[0] = lb >= p->topk ? cand[p->topk - 1].blk : (int32_t)lb;"),
     # causal clip of the local block dropped
-    "no_causal_clip": ("if (tok > t) continue;", "(void)0;"),
+    "no_causal_clip": ("if (tok > t) continue;\n          krow[n]", "(void)0;\n          krow[n]"),
     # softmax scale dropped
     "no_scale": ("z[i] = s * p->scale;\n      }\n      softmax_combine",
                  "z[i] = s;\n      }\n      softmax_combine"),
@@ -35,8 +36,8 @@ MUTANTS = {
     "wrong_kv_head": ("krow[n] = k + (size_t)tok * row + (size_t)g * p->D;\n          vrow",
                       "krow[n] = k + (size_t)tok * row + (size_t)(p->G - 1 - g) * p->D;\n          vrow"),
     # index dot product over one dimension too few
-    "dropped_index_term": ("for (int d = 0; d < p->Di; ++d) s +=",
-                           "for (int d = 1; d < p->Di; ++d) s +="),
+    "dropped_index_term": ("for (int d = 0; d < p->Di; ++d) s += bf16_to_double(qg[d])",
+                           "for (int d = 1; d < p->Di; ++d) s += bf16_to_double(qg[d])"),
     # softmax normaliser off by one
     "bad_normaliser": ("for (int d = 0; d < D; ++d) out[d] /= l;",
                        "for (int d = 0; d < D; ++d) out[d] /= (l + 1.0);"),
@@ -53,6 +54,18 @@ MUTANTS = {
     # selection quality: softmax scale dropped
     "quality_no_scale": ("z[i] = s * p->scale;\n        if (z[i] > m)",
                          "z[i] = s;\n        if (z[i] > m)"),
+    # KL: the divergence taken the other way round, D_KL(Q || P)
+    "kl_reversed": ("if (P[j] > 0.0) loss += P[j] * (log(P[j]) - log(Q[j]));",
+                    "loss += Q[j] * (log(Q[j]) - log(P[j]));"),
+    # KL: gradient of the pooled scores with the wrong sign
+    "kl_grad_sign": ("const double dz = Q[j] - P[j];", "const double dz = P[j] - Q[j];"),
+    # KL: teacher not averaged over the group's heads
+    "kl_heads_summed": ("P[j] += exp(z[i++] - m) / Z / hpg;", "P[j] += exp(z[i++] - m) / Z;"),
+    # KL: a tied pooled maximum credited to the last token
+    "kl_tie_last": ("if (s > zi[j]) { /* strictly", "if (s >= zi[j]) { /* strictly"),
+    # KL: pooled index scores of the local block include tokens after t
+    "kl_pool_not_causal": ("        if (tok > t) continue;\n        const uint16_t *kr = k_idx",
+                           "        const uint16_t *kr = k_idx"),
     # selection quality: the full softmax stops at the local block's start
     "quality_no_local_tokens": ("      for (int64_t i = 0; i <= t; ++i) {\n        const uint16_t *kr",
                                 "      for (int64_t i = 0; i < lb * p->block; ++i) {\n        const uint16_t *kr"),
@@ -70,6 +83,10 @@ PINS = [
     qpins.test_quality_short_context_recalls_everything,
     qpins.test_quality_dominant_key_closed_form,
     qpins.test_quality_ideal_selection_dominates_the_index_selection,
+    klpins.test_single_candidate_gives_zero_loss_and_gradient,
+    klpins.test_teacher_and_student_distributions,
+    klpins.test_gradients_match_finite_differences_of_the_loss,
+    klpins.test_tied_maximum_sends_the_gradient_to_the_first_token,
 ]
 
 
