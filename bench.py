@@ -244,6 +244,43 @@ class Job:
                                for c in self.calls])
 
 
+def selection_quality(job, nrows, seed=7):
+    """Attention-mass coverage and selection recall of the step's selections
+    (msa_selection_quality) on nrows seeded query positions; not timed."""
+    import torch
+    msa = job.msa
+    rng = np.random.default_rng(seed)
+    if job.w["kind"] == "decode":
+        calls = [(job.B, 0, [job.L - 1] * job.B)]
+    else:
+        pos = job.positions()
+        pick = np.sort(rng.choice(len(pos), size=min(nrows, len(pos)), replace=False))
+        calls = [(1, int(a), [int(pos[a])]) for a in pick]
+    cov, best, rec = [], [], []
+    for B, a, qs in calls:
+        p = msa.params(B, 1, H, G, D, DI, job.nb)
+        ws = msa.quality_workspace(p)
+        c = torch.empty((B, 1, H), dtype=torch.float32, device="cuda")
+        bc = torch.empty_like(c)
+        ds = torch.empty((B, 1, G, 16), dtype=torch.int32, device="cuda")
+        hits = torch.empty((B, 1, G), dtype=torch.int32, device="cuda")
+        msa.msa_selection_quality(p, job.dev["q"][:, a:a + 1], job.dev["k"], job.sel[:, a:a + 1],
+                                  qs, [t + 1 for t in qs], c, bc, ds, hits, ws)
+        nsel = np.minimum(16, np.asarray(qs) // BLK + 1)[:, None, None]
+        cov.append(c.cpu().numpy().reshape(-1))
+        best.append(bc.cpu().numpy().reshape(-1))
+        rec.append((hits.cpu().numpy() / nsel).reshape(-1))
+    cov, best, rec = np.concatenate(cov), np.concatenate(best), np.concatenate(rec)
+    return {"rows": len(calls) if job.w["kind"] != "decode" else job.B,
+            "coverage_mean": float(cov.mean()), "coverage_min": float(cov.min()),
+            "best_coverage_mean": float(best.mean()), "recall_mean": float(rec.mean()),
+            "recall_min": float(rec.min()),
+            "definition": "coverage: full causal softmax mass inside the 16 selected blocks, "
+                          "per (query, head); best: the same for the ideal selection (local "
+                          "block + top-15 by group-averaged mass); recall: |selected and "
+                          "ideal| / |ideal| per (query, group)"}
+
+
 def time_job(job, steps, warmup, world):
     import torch
     for _ in range(warmup):
@@ -563,6 +600,7 @@ def measure(name, args, world, rank):
                  "achieved_tflops": (fi + fa) / (ms / 1000.0) / 1e12,
                  "attn_achieved_tflops": fa / (att_ms / 1000.0) / 1e12}
         whole["frac_of_bf16_peak"] = whole["achieved_tflops"] / peak_tf
+    quality = selection_quality(job, args.quality_rows) if args.quality_rows > 0 else None
     e2e_ms, h2d, d2h = time_e2e(job, max(1, min(args.steps, 3)), world, args.host_alloc)
     cfg = {"workload": name, "batch": job.B, "ctx": job.L, "calls_per_step": len(job.calls),
            "queries_per_call": job.calls[0]["T"], "heads": H, "kv_heads": G, "head_dim": D,
@@ -581,7 +619,8 @@ def measure(name, args, world, rank):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "host_buffers": {"thp": "page-locked transparent huge pages",
                                      "torch": "torch pinned allocator"}[args.host_alloc]},
-            "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu}
+            "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
+            "selection_quality": quality}
 
 
 def gpu_arm(args, world, rank):
@@ -596,7 +635,7 @@ def gpu_arm(args, world, rank):
                 "with needles)",
     }
     for k in ("config", "roofline", "step", "kernels_ms", "e2e", "gpu_launches", "clocks",
-              "cpu_baseline"):
+              "cpu_baseline", "selection_quality"):
         line[k] = r[k]
     for sec in args.secondary:
         if sec == args.workload:
@@ -607,7 +646,7 @@ def gpu_arm(args, world, rank):
             "ms_per_step": s["ms_per_step"], "config": s["config"], "roofline": s["roofline"],
             "step": s["step"], "kernels_ms": s["kernels_ms"], "e2e": s["e2e"],
             "gpu_launches": s["gpu_launches"], "clocks": s["clocks"],
-            "cpu_baseline": s["cpu_baseline"]}
+            "cpu_baseline": s["cpu_baseline"], "selection_quality": s["selection_quality"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -625,9 +664,11 @@ def main():
                     help="comma-separated workloads reported in the same line (default: "
                          "prefill_128k,decode_256k when the workload is the default one; "
                          "'none' to skip)")
-    ap.add_argument("--host-alloc", choices=["thp", "torch"], default="thp",
-                    help="host buffers of the e2e leg: page-locked transparent huge pages "
-                         "(default) or torch's pinned allocator")
+    ap.add_argument("--host-alloc", choices=["thp", "torch"], default="torch",
+                    help="host buffers of the e2e leg: torch's pinned allocator (default) or "
+                         "page-locked transparent huge pages (measured slower on GB300)")
+    ap.add_argument("--quality-rows", type=int, default=64,
+                    help="query positions sampled for the selection-quality figures (0: skip)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     args = ap.parse_args()
     if args.secondary is None:

@@ -320,7 +320,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int ks = kv % kKVStages;
         const uint32_t w = (uint32_t)(kv / kKVStages);
         const int kb = d.w & 0x7FFF, g = (d.w >> 15) & 7, b = d.w >> 18;
-        const int row = (int)(((int64_t)b * a.s.max_blocks + kb) * kBlock);
+        // through the block table when the caches are paged; an entry outside
+        // the pool (flagged) reads zeros from past the pool's end
+        const int64_t pb = cache_block(a.s, b, kb, a.status);
+        const int row = (int)((pb < 0 ? a.s.cache_blocks() : pb) * kBlock);
         if (!mbar_wait(&k_empty[ks], (w & 1) ^ 1, a.status, a.wait_polls)) { *abort_flag = 1; break; }
         mbar_arrive_expect_tx(&k_full[ks], C::kSmemK);
 #pragma unroll
@@ -350,9 +353,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // S and P in TMEM columns [128c, 128c + 128), O in [256 + 128c, ...).
     // tcgen05.mma executes in issue order, so S(t + 2) cannot overwrite the P
     // that P.V(t), issued before it, still reads.
-    if (lane == 0) {
+    // The whole warp runs the loop; one elected lane issues the MMAs and
+    // commits, from descriptors formed once per ring and stepped by byte
+    // offset / 16 (measured: half the issue time of a loop run by lane 0).
+    {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
+      const uint64_t qdesc0 = smem_desc(smem_u32(sQ), 16, C::kQGroup, kSwizzle128B);
+      const uint64_t kdesc0 = smem_desc(smem_u32(sK), 16, 1024, kSwizzle128B);
+      const uint64_t vdesc0 = smem_desc(smem_u32(sV), C::kHalf, 1024, kSwizzle128B);
       int kv = -1, prev = -1;
       int pv_ks = 0;
       uint32_t pv_w = 0;
@@ -376,49 +385,58 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           w = (uint32_t)(kv / kKVStages);
           last = (t + 1 == n) || ln != lt;
           const int c = t & 1, qs = t % kQStages;
-          ok = mbar_wait(&q_full[qs], (uint32_t)(t / kQStages) & 1, a.status, a.wait_polls) &&
-               (!first || mbar_wait(&k_full[ks], w & 1, a.status, a.wait_polls));
+          const bool okl =
+              mbar_wait(&q_full[qs], (uint32_t)(t / kQStages) & 1, a.status, a.wait_polls) &&
+              (!first || mbar_wait(&k_full[ks], w & 1, a.status, a.wait_polls));
+          ok = __all_sync(0xffffffffu, okl);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t q0 = smem_u32(sQ + qs * C::kSmemQ), k0 = smem_u32(sK + ks * C::kSmemK);
+          const uint64_t qd = qdesc0 + (uint64_t)((qs * C::kSmemQ) >> 4);
+          const uint64_t kd = kdesc0 + (uint64_t)((ks * C::kSmemK) >> 4);
+          if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t kin = (k & 3) * 32;  // 16 dims within a 64-dim half
-            tc_mma_f16(tmem + c * 128,
-                       smem_desc(q0 + (k >> 2) * 1024 + kin, 16, C::kQGroup, kSwizzle128B),
-                       smem_desc(k0 + (k >> 2) * C::kHalf + kin, 16, 1024, kSwizzle128B), idesc_s,
-                       k > 0);
+            for (int k = 0; k < D / 16; ++k)  // 16 dims: (k & 3) * 32 bytes within a 64-dim half
+              tc_mma_f16(tmem + c * 128, qd + (uint64_t)(((k >> 2) * 1024 + (k & 3) * 32) >> 4),
+                         kd + (uint64_t)(((k >> 2) * C::kHalf + (k & 3) * 32) >> 4), idesc_s,
+                         k > 0);
+            tc_commit(&q_empty[qs]);
+            tc_commit(&s_full[c]);
+            if (last) tc_commit(&k_empty[ks]);
           }
-          tc_commit(&q_empty[qs]);
-          tc_commit(&s_full[c]);
-          if (last) tc_commit(&k_empty[ks]);
+          __syncwarp();
         }
         if (t >= 1) {
           // ---- P.V(t - 1)
           const int tp = t - 1, c = tp & 1;
           const uint32_t j = (uint32_t)(tp >> 1);
-          ok = mbar_wait(&p_full[c], j & 1, a.status, a.wait_polls) &&
-               (!pv_first || mbar_wait(&v_full[pv_ks], pv_w & 1, a.status, a.wait_polls)) &&
-               (j == 0 || mbar_wait(&o_empty[c], (j - 1) & 1, a.status, a.wait_polls));
+          const bool okl =
+              mbar_wait(&p_full[c], j & 1, a.status, a.wait_polls) &&
+              (!pv_first || mbar_wait(&v_full[pv_ks], pv_w & 1, a.status, a.wait_polls)) &&
+              (j == 0 || mbar_wait(&o_empty[c], (j - 1) & 1, a.status, a.wait_polls));
+          ok = __all_sync(0xffffffffu, okl);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t v0 = smem_u32(sV + pv_ks * C::kSmemK);
+          const uint64_t vd = vdesc0 + (uint64_t)((pv_ks * C::kSmemK) >> 4);
           // P (bf16, two per column) is in TMEM columns [128c, 128c + 64)
+          if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            tc_mma_f16_ts(tmem + 256 + c * 128, tmem + c * 128 + k * 8,
-                          smem_desc(v0 + k * 2048, C::kHalf, 1024, kSwizzle128B), idesc_o, k > 0);
-          tc_commit(&o_full[c]);
-          if (pv_last) tc_commit(&v_empty[pv_ks]);
+            for (int k = 0; k < 8; ++k)
+              tc_mma_f16_ts(tmem + 256 + c * 128, tmem + c * 128 + k * 8,
+                            vd + (uint64_t)((k * 2048) >> 4), idesc_o, k > 0);
+            tc_commit(&o_full[c]);
+            if (pv_last) tc_commit(&v_empty[pv_ks]);
+          }
+          __syncwarp();
         }
         pv_ks = ks;
         pv_w = w;
         pv_last = last;
         pv_first = first;
       }
-      if (!ok) *abort_flag = 1;
+      if (!ok && lane == 0) *abort_flag = 1;
       // all MMAs done before TMEM is released
-      tc_commit(bar_fin);
+      if (elect_one()) tc_commit(bar_fin);
+      __syncwarp();
       mbar_wait(bar_fin, 0, nullptr);
     }
   } else if (warp < kEpiWarp0) {
@@ -581,8 +599,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // ---- merge: one warp per (sequence, query, head) ----------------------------
-template <int D>
-__global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnPass a, uint16_t* __restrict__ out) {
+// DENSE: fold the pass's partials into the dense accumulators instead (one
+// chunk of msa_dense_attn).
+template <int D, bool DENSE>
+__global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnPass a, uint16_t* __restrict__ out,
+                                                            DenseStep ds) {
   constexpr int PER = D / 32;
   const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -630,11 +651,15 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnPass a, uint16_t
       acc[1] += wj * bf16hi(u);
     }
   }
-  const float inv = 1.f / W;
   uint16_t* dst = out + (((size_t)b * a.s.T + i) * H + h) * D + lane * PER;
+  if constexpr (DENSE) {
+    dense_fold<PER>(ds, ((size_t)b * a.s.T + i) * H + h, M, W, acc, lane, dst);
+  } else {
+    const float inv = 1.f / W;
 #pragma unroll
-  for (int e = 0; e < PER; e += 2)
-    *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+    for (int e = 0; e < PER; e += 2)
+      *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+  }
 }
 
 struct AttnLayout {
@@ -665,7 +690,8 @@ AttnLayout attn_layout(const Shape& s) {
 template <int D>
 cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint16_t* q,
                                 const uint16_t* k, const uint16_t* v, const int32_t* sel,
-                                uint16_t* out, const Workspace& ws, cudaStream_t st) {
+                                uint16_t* out, const Workspace& ws, cudaStream_t st,
+                                const DenseStep* dense) {
   using C = AttnCfg<D>;
   const AttnLayout lay = attn_layout(s);
   char* base = ws.tc_base;
@@ -682,8 +708,7 @@ cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint
       return cudaErrorInvalidValue;
   }
   {
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)s.G,
-                          (cuuint64_t)s.B * s.max_blocks * kBlock};
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)s.G, (cuuint64_t)(s.cache_blocks() * kBlock)};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)s.G * D * 2};
     cuuint32_t box[3] = {64, 1, (cuuint32_t)kBlock};
     if (!encode_bf16_map(&tm_k, k, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -730,7 +755,11 @@ cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint
     attn_tc_kernel<D><<<grid, kAttnThreads, C::kSmem, st>>>(tm_q, tm_k, tm_v, a);
     const int64_t warps = (int64_t)s.B * a.Tp * s.H;
     note_launches(1);
-    attn_tc_merge_kernel<D><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(a, out);
+    if (dense)
+      attn_tc_merge_kernel<D, true><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(a, out, *dense);
+    else
+      attn_tc_merge_kernel<D, false><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(a, out,
+                                                                                 DenseStep{});
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -748,9 +777,10 @@ size_t tc_attn_workspace_bytes(const Shape& s) { return attn_layout(s).total; }
 
 cudaError_t launch_attn_tc(const Shape& s, const Positions& pos, const uint16_t* q,
                            const uint16_t* k, const uint16_t* v, const int32_t* sel,
-                           uint16_t* out, const Workspace& ws, cudaStream_t st) {
-  if (s.D == 128) return launch_attn_tc_impl<128>(s, pos, q, k, v, sel, out, ws, st);
-  return launch_attn_tc_impl<64>(s, pos, q, k, v, sel, out, ws, st);
+                           uint16_t* out, const Workspace& ws, cudaStream_t st,
+                           const DenseStep* dense) {
+  if (s.D == 128) return launch_attn_tc_impl<128>(s, pos, q, k, v, sel, out, ws, st, dense);
+  return launch_attn_tc_impl<64>(s, pos, q, k, v, sel, out, ws, st, dense);
 }
 
 }  // namespace msa

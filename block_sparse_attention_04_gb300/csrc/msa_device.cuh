@@ -156,9 +156,36 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
-// Records an invalid selected id in the status word unless a timeout (which
-// takes precedence) is already recorded.
-__device__ __forceinline__ void flag_invalid(int* status) { atomicCAS(status, 0, kDevInvalid); }
+// Records an invalid selected id (or block-table entry) in the status word
+// unless a timeout (which takes precedence) is already recorded.
+__device__ __forceinline__ void flag_invalid(int* status) {
+  if (status) atomicCAS(status, 0, kDevInvalid);
+}
+
+// The cache block holding logical block kb of sequence b: through the block
+// table for paged caches, b * max_blocks + kb otherwise.  A table entry
+// outside the pool is flagged and -1 returned; the caller then reads nothing
+// from the cache for that block.
+__device__ __forceinline__ int64_t cache_block(const Shape& s, int b, int kb, int* status) {
+  if (!s.bt) return (int64_t)b * s.max_blocks + kb;
+  const int pb = __ldg(s.bt + (size_t)b * s.max_blocks + kb);
+  if (pb < 0 || pb >= s.pool_blocks) {
+    flag_invalid(status);
+    return -1;
+  }
+  return pb;
+}
+
+// One lane of a converged warp, chosen by the hardware (elect.sync).  The
+// single-thread tcgen05 instructions are issued from inside such a branch, so
+// that the warp stays converged and their operands are warp-uniform values.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n selp.u32 %0, 1, 0, P;\n}"
+      : "=r"(pred));
+  return pred != 0;
+}
 
 // --------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void tma_load_2d(uint32_t sdst, const void* tmap, uint64_t* bar,
@@ -361,6 +388,37 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          | ((b_mn ? 1u : 0u) << 16)      // B major
          | ((uint32_t)(N >> 3) << 17)    // N / 8
          | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// Dense attention: folds one chunk into the running accumulator (see
+// DenseStep).  Mc = -inf means the chunk held no causal block for this query.
+template <int PER>
+__device__ __forceinline__ void dense_fold(const DenseStep& ds, size_t acc_row, float Mc, float Wc,
+                                           float (&oc)[PER], int lane, uint16_t* dst) {
+  float* ao = ds.acc_o + acc_row * (32 * PER) + lane * PER;
+  float am = -INFINITY, al = 0.f;
+  if (!ds.first) {
+    const float2 ml = ds.acc_ml[acc_row];
+    am = ml.x;
+    al = ml.y;
+  }
+  const float M = fmaxf(am, Mc);
+  const float wa = am == -INFINITY ? 0.f : ex2(am - M);
+  const float wc = Mc == -INFINITY ? 0.f : ex2(Mc - M);
+  float o[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) o[e] = (ds.first ? 0.f : ao[e] * wa) + oc[e] * wc;
+  const float L = al * wa + Wc * wc;
+  if (ds.last) {
+    const float inv = 1.f / L;
+#pragma unroll
+    for (int e = 0; e < PER; e += 2)
+      *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(o[e] * inv, o[e + 1] * inv);
+  } else {
+#pragma unroll
+    for (int e = 0; e < PER; ++e) ao[e] = o[e];
+    if (lane == 0) ds.acc_ml[acc_row] = make_float2(M, L);
+  }
 }
 
 }  // namespace msa

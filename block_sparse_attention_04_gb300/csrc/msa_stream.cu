@@ -51,7 +51,7 @@ template <int DI>
 __global__ void __launch_bounds__(kIdxWarps * 32) index_stream_kernel(
     Shape s, Positions pos, int T, int t0, int Tp, int bps, int nsplit,
     const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_idx,
-    Cand* __restrict__ cand) {
+    Cand* __restrict__ cand, int* __restrict__ status) {
   constexpr int NJ = DI / 16;  // mma k-steps per key row
   constexpr int NU = DI / 32;  // 16-byte loads per key row and thread
   __shared__ float pooled[kMaxBps][8];
@@ -83,7 +83,6 @@ __global__ void __launch_bounds__(kIdxWarps * 32) index_stream_kernel(
     }
   }
 
-  const uint16_t* kseq = k_idx + (size_t)b * s.max_blocks * kBlock * DI;
   // This warp's blocks are blk0 + warp + k * kIdxWarps, streamed in steps of
   // 16 key rows (8 steps per block).  The loads of step it + 1 are issued
   // before the MMAs of step it, so each warp keeps two steps in flight
@@ -93,10 +92,13 @@ __global__ void __launch_bounds__(kIdxWarps * 32) index_stream_kernel(
   const int nbw = (blk1 - blk0 - warp + kIdxWarps - 1) / kIdxWarps;
   const int n = nbw > 0 ? nbw * SPB : 0;
   uint4 C0[NU], C1[NU];  // rows gq and gq + 8 of the current step
+  // (a block-table entry outside the pool is flagged and block 0 read instead)
 #define MSA_IDX_LOAD(IT, X0, X1)                                                        \
   do {                                                                                  \
     const int blk_ = blk0 + warp + ((IT) / SPB) * kIdxWarps;                            \
-    const uint16_t* r_ = kseq + ((size_t)blk_ * kBlock + ((IT) % SPB) * 16 + gq) * DI;  \
+    const int64_t pb_ = cache_block(s, b, blk_, status);                                \
+    const uint16_t* r_ =                                                                \
+        k_idx + ((size_t)(pb_ < 0 ? 0 : pb_) * kBlock + ((IT) % SPB) * 16 + gq) * DI;    \
     _Pragma("unroll") for (int u_ = 0; u_ < NU; ++u_) {                                 \
       X0[u_] = ldg_stream(r_ + (tq + 4 * u_) * 8);                                      \
       X1[u_] = ldg_stream(r_ + 8 * DI + (tq + 4 * u_) * 8);                             \
@@ -309,6 +311,14 @@ __global__ void __launch_bounds__(128) attn_stream_kernel(
     if (threadIdx.x == 0) flag_invalid(status);
     kb = -1;
   }
+  int64_t pb = -1;   // the cache block holding it
+  if (kb >= 0) {
+    pb = cache_block(s, b, kb, nullptr);
+    if (pb < 0) {
+      if (threadIdx.x == 0) flag_invalid(status);
+      kb = -1;
+    }
+  }
   if (kb < 0) {
     for (int h = threadIdx.x; h < hpg; h += blockDim.x) {
       part_ml[(ml_base + (size_t)h * kTopk) * 2 + 0] = -INFINITY;
@@ -318,8 +328,8 @@ __global__ void __launch_bounds__(128) attn_stream_kernel(
   }
 
   const size_t tok_stride = (size_t)G * D;
-  const uint16_t* kblk = kc + ((size_t)b * s.max_blocks + kb) * kBlock * tok_stride + (size_t)g * D;
-  const uint16_t* vblk = vc + ((size_t)b * s.max_blocks + kb) * kBlock * tok_stride + (size_t)g * D;
+  const uint16_t* kblk = kc + (size_t)pb * kBlock * tok_stride + (size_t)g * D;
+  const uint16_t* vblk = vc + (size_t)pb * kBlock * tok_stride + (size_t)g * D;
 
   // scores S^T[token][head] for this warp's 32 tokens
   float sc[2][NTH][4];
@@ -476,10 +486,11 @@ __global__ void __launch_bounds__(128) attn_stream_kernel(
 
 // ---------------------------------------------------------------------------
 // attn_merge: one warp per (pass row, head).
-template <int D>
+// DENSE: fold into the dense accumulators instead (one chunk of msa_dense_attn).
+template <int D, bool DENSE>
 __global__ void __launch_bounds__(256) attn_merge_kernel(
     Shape s, int T, int t0, int Tp, int nrows, const float* __restrict__ part_o,
-    const float* __restrict__ part_ml, uint16_t* __restrict__ out) {
+    const float* __restrict__ part_ml, uint16_t* __restrict__ out, DenseStep ds) {
   constexpr int PER = D / 32;
   const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -509,11 +520,30 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] += wj * src[e];
   }
-  const float inv = 1.f / L;
   uint16_t* dst = out + ((size_t)(b * T + i) * s.H + h) * D + lane * PER;
+  if constexpr (DENSE) {
+    dense_fold<PER>(ds, (size_t)(b * T + i) * s.H + h, M, L, acc, lane, dst);
+  } else {
+    const float inv = 1.f / L;
 #pragma unroll
-  for (int e = 0; e < PER; e += 2) {
-    *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+    for (int e = 0; e < PER; e += 2) {
+      *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+    }
+  }
+}
+
+// Dense attention, chunk c: blocks 16c .. 16c+15 of every query, those past
+// its local block as -1.
+__global__ void dense_sel_kernel(Shape s, Positions pos, int chunk, int32_t* __restrict__ sel) {
+  const int64_t n = (int64_t)s.B * s.T * s.G * kTopk;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int j = (int)(e % kTopk);
+    const int64_t r = e / kTopk / s.G;       // b * T + i
+    const int b = (int)(r / s.T), i = (int)(r % s.T);
+    const int64_t lb = ((int64_t)pos.q_start[b] + i) / kBlock;
+    const int64_t kb = (int64_t)chunk * kTopk + j;
+    sel[e] = kb <= lb ? (int32_t)kb : -1;
   }
 }
 
@@ -629,10 +659,10 @@ cudaError_t launch_index_stream(const Shape& s, const Positions& pos, int t0, in
     dim3 grid(nsplit, rows);
     if (s.Di == 64)
       index_stream_kernel<64><<<grid, kIdxWarps * 32, 0, st>>>(s, pos, s.T, t0, Tp, bps, nsplit,
-                                                               q_idx, k_idx, ws.cand);
+                                                               q_idx, k_idx, ws.cand, ws.status);
     else
       index_stream_kernel<32><<<grid, kIdxWarps * 32, 0, st>>>(s, pos, s.T, t0, Tp, bps, nsplit,
-                                                               q_idx, k_idx, ws.cand);
+                                                               q_idx, k_idx, ws.cand, ws.status);
   }
   return launch_topk_merge(s, pos, t0, t1, bps, nsplit > 0 ? nsplit : 1, ws.cand, sel, st);
 }
@@ -654,10 +684,21 @@ cudaError_t launch_topk_merge(const Shape& s, const Positions& pos, int t0, int 
   return cudaGetLastError();
 }
 
+cudaError_t launch_dense_sel(const Shape& s, const Positions& pos, int chunk, int32_t* sel,
+                             cudaStream_t st) {
+  const int64_t n = (int64_t)s.B * s.T * s.G * kTopk;
+  if (n == 0) return cudaSuccess;
+  const int64_t blocks = (n + 255) / 256;
+  note_launches(1);
+  dense_sel_kernel<<<(unsigned)(blocks < 65536 ? blocks : 65536), 256, 0, st>>>(s, pos, chunk,
+                                                                               sel);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_stream(const Shape& s, const Positions& pos, int t0, int t1,
                                const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                const int32_t* sel, uint16_t* out, const Workspace& ws,
-                               cudaStream_t st) {
+                               cudaStream_t st, const DenseStep* dense) {
   const int Tp = t1 - t0;
   const int rows = s.B * Tp;
   if (rows <= 0) return cudaSuccess;
@@ -674,12 +715,20 @@ cudaError_t launch_attn_stream(const Shape& s, const Positions& pos, int t0, int
   }
 #undef MSA_ATTN_STREAM
   const int warps = rows * s.H;
-  if (s.D == 128)
-    attn_merge_kernel<128><<<(warps + 7) / 8, 256, 0, st>>>(s, s.T, t0, Tp, rows, ws.part_o,
-                                                           ws.part_ml, out);
-  else
-    attn_merge_kernel<64><<<(warps + 7) / 8, 256, 0, st>>>(s, s.T, t0, Tp, rows, ws.part_o,
-                                                          ws.part_ml, out);
+  const DenseStep ds = dense ? *dense : DenseStep{};
+#define MSA_ATTN_MERGE(DD)                                                                       \
+  if (dense)                                                                                     \
+    attn_merge_kernel<DD, true><<<(warps + 7) / 8, 256, 0, st>>>(s, s.T, t0, Tp, rows, ws.part_o, \
+                                                                 ws.part_ml, out, ds);           \
+  else                                                                                           \
+    attn_merge_kernel<DD, false><<<(warps + 7) / 8, 256, 0, st>>>(s, s.T, t0, Tp, rows,          \
+                                                                  ws.part_o, ws.part_ml, out, ds)
+  if (s.D == 128) {
+    MSA_ATTN_MERGE(128);
+  } else {
+    MSA_ATTN_MERGE(64);
+  }
+#undef MSA_ATTN_MERGE
   return cudaGetLastError();
 }
 

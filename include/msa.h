@@ -34,7 +34,7 @@
  *     0 <= q_start[b], q_start[b] + T <= kv_len[b] <= max_blocks*128.
  *     Prefill: q_start = 0, kv_len = T.  Chunked prefill: q_start = chunk
  *     start.  Decode: T = 1, q_start = kv_len - 1 (the new token's K, V and
- *     K_idx are already in the caches).
+ *     K_idx are already in the caches: msa_cache_append writes them).
  *   - ws is caller-owned device scratch of at least msa_workspace_bytes(p)
  *     bytes, 256-byte aligned.  The library never allocates memory and keeps
  *     no state between calls except a status word inside ws.
@@ -126,6 +126,47 @@ int msa_forward(const msa_params *p, const uint16_t *q_idx, const uint16_t *k_id
                 const int32_t *q_start, const int32_t *kv_len, int32_t *sel_out,
                 uint16_t *out, void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/* ---- Paged caches --------------------------------------------------------
+ * "前沿架构解码手记（三）：MiniMax M2.7 → M3", section 2.1 ("KV-Block-Major
+ * Prefill") keeps the KV cache block -> token -> head -> dim so that every
+ * block a query selects is one contiguous run, and names this layout as what
+ * lets paged serving engines run MSA unchanged.  Here the pages of such an
+ * engine are exactly MSA's 128-token blocks: the K, V and K_idx of all
+ * sequences live in pools of num_pool_blocks blocks,
+ *     k_pool, v_pool  [num_pool_blocks][128][G][D]     bf16
+ *     k_idx_pool      [num_pool_blocks][128][Di]       bf16
+ * and block_table[B][max_blocks] (device int32) maps logical block kb of
+ * sequence b (its tokens kb*128 .. kb*128+127) to a pool block.  Entries of
+ * blocks a call never reaches are not read.  An entry that is read and lies
+ * outside [0, num_pool_blocks) is not dereferenced: the kernels record
+ * MSA_ERR_INVALID_ARG in ws (msa_workspace_status) and use zeros instead.
+ * num_pool_blocks * 128 must stay below 2^31 - 128 (MSA_ERR_UNSUPPORTED). */
+
+/* Appends p->T new tokens to every sequence's caches: the token of row i of
+ * sequence b goes to position q_start[b] + i (host array), i.e. row
+ * (q_start[b] + i) % 128 of logical block (q_start[b] + i) / 128.
+ *   k_new, v_new [B][T][G][D] bf16, k_idx_new [B][T][Di] bf16 (device)
+ * block_table NULL: the caches are per sequence (msa_forward's layout,
+ * [B][max_blocks][128][...]) and num_pool_blocks is ignored; otherwise they
+ * are the pools above.  Requires 0 <= q_start[b], q_start[b] + T <=
+ * max_blocks * 128.  ws: at least 256 bytes of device scratch (256-byte
+ * aligned) that receives the status word.  Only the rows written change. */
+int msa_cache_append(const msa_params *p, const int32_t *block_table, int num_pool_blocks,
+                     const uint16_t *k_new, const uint16_t *v_new, const uint16_t *k_idx_new,
+                     const int32_t *q_start, uint16_t *k_cache, uint16_t *v_cache,
+                     uint16_t *k_idx_cache, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* msa_forward over paged caches: the same steps, arguments and results, with
+ * k_idx, k_cache and v_cache replaced by the pools and every cache block read
+ * through block_table (both kernel families).  ws as for msa_forward
+ * (msa_workspace_bytes(p)).  Decode appends the new token first
+ * (msa_cache_append), then calls this with q_start = kv_len - 1. */
+int msa_forward_paged(const msa_params *p, const int32_t *block_table, int num_pool_blocks,
+                      const uint16_t *q_idx, const uint16_t *k_idx_pool, const uint16_t *q,
+                      const uint16_t *k_pool, const uint16_t *v_pool, const int32_t *q_start,
+                      const int32_t *kv_len, int32_t *sel_out, uint16_t *out, void *ws,
+                      size_t ws_bytes, cudaStream_t stream);
+
 /* msa_index_topk for callers that cannot allocate device memory.  The pages
  * have no counterpart: this is a deployment variant of steps 1-3, not part
  * of the method.
@@ -158,6 +199,76 @@ int msa_forward(const msa_params *p, const uint16_t *q_idx, const uint16_t *k_id
 int msa_index_topk_noalloc(const msa_params *p, const uint16_t *q_idx, const uint16_t *k_idx,
                            const int32_t *q_start, const int32_t *kv_len, int32_t *sel,
                            cudaStream_t stream);
+
+/* Dense causal GQA attention over the same block-major caches: every query
+ * head attends every token <= t of its group's KV head (the full-attention
+ * equation of "MiniMax 模型迭代与竞品分析" section 2, without selection).
+ * M3 keeps its first three layers dense (section 3 of the same page:
+ * sparse_attention_freq starts with three zeros), so a model built on this
+ * library runs those layers here, on the caches its MSA layers use.  The
+ * blocks are processed in chunks of 16 through the same attention kernels as
+ * msa_sparse_attn (tensor-core KV-outer for prefill-sized calls, streaming
+ * otherwise), each chunk's block partials folded into fp32 running
+ * (output, max, sum) accumulators; out is bf16 (round to nearest even).
+ * Arguments as for msa_sparse_attn without sel; ws of at least
+ * msa_dense_workspace_bytes(p) bytes, 256-byte aligned (it holds
+ * B*T*H*(D+2) fp32 accumulators besides the attention scratch). */
+size_t msa_dense_workspace_bytes(const msa_params *p);
+int msa_dense_attn(const msa_params *p, const uint16_t *q, const uint16_t *k_cache,
+                   const uint16_t *v_cache, const int32_t *q_start, const int32_t *kv_len,
+                   uint16_t *out, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* The index branch's training signal ("MiniMax 模型迭代与竞品分析" section 2,
+ * the paragraph on how the indexer learns to select): over the candidate
+ * blocks C of each (query, group) -- the distinct ids of sel in [0, lb] --
+ *   P_j  the main branch's softmax mass on block j (the sparse softmax over
+ *        the selected tokens <= t), averaged over the group's heads; the
+ *        teacher, so no gradient flows into q or k_cache
+ *   z_j  the block's pooled index score, max over its tokens <= t of
+ *        <Q_idx, K_idx[tok]>, first attained at token a_j
+ *   Q_j  exp(z_j) / sum over C of exp(z_c)      (the student)
+ * Outputs (fp32, device, caller-owned):
+ *   kl[B][T][G]          D_KL(P || Q) = sum_j P_j (ln P_j - ln Q_j)
+ *   dq_idx[B][T][G][Di]  the gradient of the summed loss with respect to Q_idx:
+ *                        sum_j (Q_j - P_j) K_idx[a_j]            (written)
+ *   dk_idx[B][max_blocks*128][Di]  its gradient with respect to K_idx:
+ *                        (Q_j - P_j) Q_idx added at row a_j with atomic adds
+ *                        (accumulated: the caller zeroes it first)
+ * Pooled scores accumulate in fp32, exact for inputs on a 2^-3 grid.  ws: at
+ * least msa_index_kl_workspace_bytes(p) bytes, 256-byte aligned. */
+size_t msa_index_kl_workspace_bytes(const msa_params *p);
+int msa_index_kl(const msa_params *p, const uint16_t *q_idx, const uint16_t *k_idx,
+                 const uint16_t *q, const uint16_t *k_cache, const int32_t *sel,
+                 const int32_t *q_start, const int32_t *kv_len, float *kl, float *dq_idx,
+                 float *dk_idx, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Selection quality: how much of the attention a selection recalls, the
+ * evaluation the same section asks for when it names the indexer's recall as
+ * MSA's risk (a block the indexer misses cannot be read by the main branch).
+ * For every (query, group) of the call, with A_h(b) the mass of block b (its
+ * tokens <= t) under head h's FULL causal softmax over tokens 0..t:
+ *   coverage[B][T][H]       sum of A_h(b) over the distinct ids of sel[b,t,g]
+ *                           that lie in [0, lb] (others are ignored)
+ *   dense_sel[B][T][G][16]  the ideal selection under the same rule: lb plus
+ *                           the top min(16, lb+1)-1 blocks b < lb by the
+ *                           group-averaged mass P(b) = mean over the group's
+ *                           heads of A_h(b), ties to the lower id; ascending,
+ *                           -1 padded
+ *   best_coverage[B][T][H]  sum of A_h(b) over dense_sel
+ *   hits[B][T][G]           |sel intersected with dense_sel|; selection recall
+ *                           is hits / min(16, lb+1)
+ * coverage and best_coverage are fp32 (scores of the bf16 inputs accumulate
+ * in fp32); all four outputs are caller-owned device memory.  q, k_cache, sel,
+ * q_start and kv_len are as in msa_sparse_attn.  ws: device scratch of at
+ * least msa_quality_workspace_bytes(p) bytes, 256-byte aligned (it scales
+ * with min(64, B*T) rows x G x max_blocks x (H/G + 1) x 8 bytes).  The cost
+ * is that of dense attention scores over the whole context: meant for
+ * sampled queries, not for every query of a long prefill. */
+size_t msa_quality_workspace_bytes(const msa_params *p);
+int msa_selection_quality(const msa_params *p, const uint16_t *q, const uint16_t *k_cache,
+                          const int32_t *sel, const int32_t *q_start, const int32_t *kv_len,
+                          float *coverage, float *best_coverage, int32_t *dense_sel,
+                          int32_t *hits, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Waits for `stream`, then returns the status the last call on ws left in
  * it: MSA_OK; MSA_ERR_TIMEOUT if a kernel's bounded wait ran out (its

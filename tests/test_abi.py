@@ -178,3 +178,52 @@ def test_large_single_prefill_call_is_accepted(lib):
     assert n >= cand + T * 8 * 16 * 4
     assert call_index(p, q_start=(0,), kv_len=(T,), ws_bytes=n - 1) == WORKSPACE
     assert call_index(p, q_start=(1,), kv_len=(T,), ws_bytes=n) == INVALID
+
+
+def test_paged_entry_points_validate_on_the_host(lib):
+    L = msa.load()
+    p = P(T=0, max_blocks=4)
+    qs = (ctypes.c_int32 * 1)(0)
+    kl = (ctypes.c_int32 * 1)(0)
+    n = msa.msa_workspace_bytes(p)
+    a, bt = 0x100000, 0x200000
+    fwd = L.msa_forward_paged
+    assert fwd(ctypes.byref(p), bt, 10, a, a, a, a, a, qs, kl, None, a, a, n, None) == OK
+    assert fwd(ctypes.byref(p), None, 10, a, a, a, a, a, qs, kl, None, a, a, n, None) == INVALID
+    assert fwd(ctypes.byref(p), bt, 0, a, a, a, a, a, qs, kl, None, a, a, n, None) == INVALID
+    assert fwd(ctypes.byref(p), bt + 2, 10, a, a, a, a, a, qs, kl, None, a, a, n, None) == INVALID
+    assert fwd(ctypes.byref(p), bt, 1 << 24, a, a, a, a, a, qs, kl, None, a, a, n,
+               None) == UNSUPPORTED
+    assert fwd(ctypes.byref(p), bt, 10, a, None, a, a, a, qs, kl, None, a, a, n, None) == INVALID
+    app = L.msa_cache_append
+    p1 = P(T=3, max_blocks=4)
+    ok_qs = (ctypes.c_int32 * 1)(4 * 128 - 3)
+    bad_qs = (ctypes.c_int32 * 1)(4 * 128 - 2)                  # runs past the capacity
+    z = P(T=0, max_blocks=4)
+    assert app(ctypes.byref(z), None, 0, a, a, a, ok_qs, a, a, a, a, 256, None) == OK
+    assert app(ctypes.byref(p1), None, 0, a, a, a, bad_qs, a, a, a, a, 256, None) == INVALID
+    assert app(ctypes.byref(p1), bt, 0, a, a, a, ok_qs, a, a, a, a, 256, None) == INVALID
+    assert app(ctypes.byref(p1), None, 0, a, a, a, ok_qs, a, a, a, a, 255, None) == WORKSPACE
+    assert app(ctypes.byref(p1), None, 0, a, a + 8, a, ok_qs, a, a, a, a, 256, None) == INVALID
+    assert app(ctypes.byref(p1), None, 0, a, a, a, None, a, a, a, a, 256, None) == INVALID
+
+
+def test_dense_entry_point_validates_on_the_host(lib):
+    L = msa.load()
+    p = P(T=0, max_blocks=4)
+    qs = (ctypes.c_int32 * 1)(0)
+    kl = (ctypes.c_int32 * 1)(0)
+    n = msa.msa_dense_workspace_bytes(p)
+    assert n > 0 and msa.msa_dense_workspace_bytes(P(D=96)) == 0
+    p1 = P(T=64, max_blocks=4)
+    assert msa.msa_dense_workspace_bytes(p1) >= 64 * 48 * (128 + 2) * 4   # fp32 accumulators
+    a = 0x100000
+    f = L.msa_dense_attn
+    assert f(ctypes.byref(p), a, a, a, qs, kl, a, a, n, None) == OK
+    assert f(ctypes.byref(p), a, None, a, qs, kl, a, a, n, None) == INVALID
+    assert f(ctypes.byref(p), a, a, a + 2, qs, kl, a, a, n, None) == INVALID
+    assert f(ctypes.byref(p), a, a, a, qs, kl, a, a + 16, n, None) == INVALID
+    qs1 = (ctypes.c_int32 * 1)(0)
+    kl1 = (ctypes.c_int32 * 1)(64)
+    n1 = msa.msa_dense_workspace_bytes(p1)
+    assert f(ctypes.byref(p1), a, a, a, qs1, kl1, a, a, n1 - 1, None) == WORKSPACE
