@@ -44,6 +44,12 @@ WORKLOADS = {
     "decode_small": dict(cfg=3, kind="decode", B=8, L=131072),
     "prefill_1m_last_chunk": dict(cfg=4, kind="prefill", B=1, L=1048576, chunk=8192,
                                   only_last=True),
+    # the rows built next to the path, measured on the same shapes:
+    # dense causal attention over a 32K prefill (msa_dense_attn), and the
+    # decode batch served from paged pools (msa_cache_append of the new token,
+    # then msa_forward_paged through a shuffled block table)
+    "dense_32k": dict(cfg=1, kind="prefill", B=1, L=32768, chunk=32768, mode="dense"),
+    "decode_256k_paged": dict(cfg=3, kind="decode", B=64, L=262144, mode="paged"),
 }
 DEFAULT_WORKLOAD = "prefill_1m"
 # measured in the same run and nested in the default line, under these keys
@@ -70,6 +76,11 @@ def index_flops(t):
 
 def attn_flops(t):
     return float(np.sum(4.0 * D * H * attended_tokens(t)))
+
+
+def dense_flops(t):
+    """Dense causal attention: 4*D*H per (query, token <= t)."""
+    return float(np.sum(4.0 * D * H * (np.asarray(t, np.int64) + 1)))
 
 
 def decode_bytes(B, L):
@@ -194,8 +205,22 @@ class Job:
         self.dev = sd.make_inputs(self.B, H, G, D, DI, self.nb, self.L, self.seed, q_rows=qrows,
                                   b0=b0)
         T = self.calls[0]["T"]
+        self.mode = w.get("mode", "sparse")
         self.params = msa.params(self.B, T, H, G, D, DI, self.nb)
-        self.ws = msa.workspace(self.params)
+        self.ws = msa.dense_workspace(self.params) if self.mode == "dense" else \
+            msa.workspace(self.params)
+        if self.mode == "paged":
+            # the caches become one pool of B * nb blocks behind a shuffled
+            # table; the newest token of each sequence is appended every step
+            g = torch.Generator().manual_seed(self.seed)
+            self.npool = self.B * self.nb
+            self.table = torch.randperm(self.npool, generator=g).to(torch.int32).reshape(
+                self.B, self.nb).cuda()
+            pos = self.L - 1
+            rows = self.table[:, pos // BLK].long() * BLK + pos % BLK
+            self.k_new = self.dev["k"].reshape(-1, G, D)[rows].reshape(self.B, 1, G, D).clone()
+            self.v_new = self.dev["v"].reshape(-1, G, D)[rows].reshape(self.B, 1, G, D).clone()
+            self.kidx_new = self.dev["k_idx"].reshape(-1, DI)[rows].reshape(self.B, 1, DI).clone()
         self.sel = torch.empty((self.B, qrows[1] - qrows[0], G, 16), dtype=torch.int32,
                                device="cuda")
         self.out = torch.empty((self.B, qrows[1] - qrows[0], H, D), dtype=torch.int16,
@@ -220,6 +245,8 @@ class Job:
         """Enqueue one step; ev: list to which (start, mid, end) events are appended."""
         import torch
         msa = self.msa
+        if self.mode != "sparse":
+            return self.step_other(ev)
         for c in self.calls:
             q_idx, k_idx, q, k, v, sel, out = self.views(c)
             if ev is not None:
@@ -231,6 +258,30 @@ class Job:
             msa.msa_sparse_attn(self.params, q, k, v, sel, c["q_start"], c["kv_len"], out,
                                 self.ws)
             if ev is not None:
+                e[2].record()
+                ev.append(e)
+
+    def step_other(self, ev):
+        """Dense attention, or the paged decode step (append, then forward)."""
+        import torch
+        msa = self.msa
+        for c in self.calls:
+            q_idx, k_idx, q, k, v, sel, out = self.views(c)
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)] if ev is not None else None
+            if e:
+                e[0].record()
+            if self.mode == "paged":
+                msa.msa_cache_append(self.params, self.k_new, self.v_new, self.kidx_new,
+                                     c["q_start"], k, v, k_idx, self.ws, block_table=self.table,
+                                     num_pool_blocks=self.npool)
+            if e:
+                e[1].record()
+            if self.mode == "dense":
+                msa.msa_dense_attn(self.params, q, k, v, c["q_start"], c["kv_len"], out, self.ws)
+            else:
+                msa.msa_forward_paged(self.params, self.table, self.npool, q_idx, k_idx, q, k, v,
+                                      c["q_start"], c["kv_len"], out, self.ws, sel_out=sel)
+            if e:
                 e[2].record()
                 ev.append(e)
 
@@ -448,6 +499,7 @@ class OracleSample:
         self.nthreads = nthreads or (os.cpu_count() or 1)
         self.d = oracle.dims(H, G, D, DI)
         self.nb = w["L"] // BLK
+        self.dense = w.get("mode") == "dense"
         rng = np.random.default_rng(self.seed)
         if w["kind"] == "decode":
             nseq = rows or 16
@@ -482,6 +534,18 @@ class OracleSample:
         """Returns (tokens_per_s, timed seconds)."""
         from concurrent.futures import ThreadPoolExecutor
         o, d = self.oracle, self.d
+        if self.dense:
+            # dense attention over every token <= t (the caches, made once)
+            if not self.kv:
+                syn = self.syn
+                self.kv[0] = (syn.kv_cache(self.seed, syn.TID_K, 0, self.nb, G, D),
+                              syn.kv_cache(self.seed, syn.TID_V, 0, self.nb, G, D))
+            kc, vc = self.kv[0]
+            t0 = time.perf_counter()
+            with ThreadPoolExecutor(self.nthreads) as ex:
+                list(ex.map(lambda r: o.dense(d, r[1], self.q[r], kc, vc), self.rows))
+            secs = time.perf_counter() - t0
+            return len(self.rows) / secs, secs
         t0 = time.perf_counter()
         with ThreadPoolExecutor(self.nthreads) as ex:
             sels = list(ex.map(lambda r: o.select(d, r[1], self.qidx[r], self.kidx[r[0]]),
@@ -571,7 +635,29 @@ def measure(name, args, world, rank):
     tokens = job.tokens() * world
     w = job.w
     pos = job.positions()
-    if w["kind"] == "decode":
+    if job.mode == "dense":
+        fa = dense_flops(pos) * job.B
+        sustained = ms * args.steps > 1000
+        peak_tf = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "kernel": "dense attention (msa_dense_attn: 16-block chunks "
+                "through attn_tc_kernel + dense merge)",
+                "achieved": fa / (att_ms / 1000.0) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
+                "traffic": None, "peak_kind": peak_kind + (" sustained" if sustained else " burst"),
+                "flops_per_step": fa}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        whole = {"flops_per_step": fa, "achieved_tflops": fa / (ms / 1000.0) / 1e12}
+    elif job.mode == "paged":
+        kidx_b, rest_b = decode_bytes(job.B, job.L)
+        app_b = job.B * 2 * (2 * G * D + DI) * 2     # read and write of the new rows
+        step_b = kidx_b + rest_b + app_b
+        roof = {"bound": "hbm", "kernel": "paged decode step (msa_cache_append + "
+                "msa_forward_paged through the block table)",
+                "achieved": step_b / (ms / 1000.0) / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "traffic": None, "peak_kind": peak_kind,
+                "bytes_per_step": step_b}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        whole = {"bytes_per_step": step_b, "append_ms": idx_ms, "forward_ms": att_ms}
+    elif w["kind"] == "decode":
         kidx_b, rest_b = decode_bytes(job.B, job.L)
         roof = {"bound": "hbm",
                 "kernel": "index scan (msa_index_topk: index_stream + topk_merge)",
@@ -600,8 +686,12 @@ def measure(name, args, world, rank):
                  "achieved_tflops": (fi + fa) / (ms / 1000.0) / 1e12,
                  "attn_achieved_tflops": fa / (att_ms / 1000.0) / 1e12}
         whole["frac_of_bf16_peak"] = whole["achieved_tflops"] / peak_tf
-    quality = selection_quality(job, args.quality_rows) if args.quality_rows > 0 else None
-    e2e_ms, h2d, d2h = time_e2e(job, max(1, min(args.steps, 3)), world, args.host_alloc)
+    quality = selection_quality(job, args.quality_rows) \
+        if args.quality_rows > 0 and job.mode == "sparse" else None
+    if job.mode == "sparse":
+        e2e_ms, h2d, d2h = time_e2e(job, max(1, min(args.steps, 3)), world, args.host_alloc)
+    else:
+        e2e_ms, h2d, d2h = None, 0, 0
     cfg = {"workload": name, "batch": job.B, "ctx": job.L, "calls_per_step": len(job.calls),
            "queries_per_call": job.calls[0]["T"], "heads": H, "kv_heads": G, "head_dim": D,
            "index_dim": DI, "block": BLK, "topk": 16, "l2": "inputs larger than L2 (no flush)"}
@@ -615,10 +705,11 @@ def measure(name, args, world, rank):
                "sample": smp.desc, "seconds": secs}
     return {"value": tokens / (ms / 1000.0), "ms_per_step": ms, "config": cfg, "roofline": roof,
             "step": whole, "kernels_ms": {"index_topk": idx_ms, "sparse_attn": att_ms},
-            "e2e": {"value": tokens / (e2e_ms / 1000.0), "unit": "tokens/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "host_buffers": {"thp": "page-locked transparent huge pages",
-                                     "torch": "torch pinned allocator"}[args.host_alloc]},
+            "e2e": None if e2e_ms is None else {
+                "value": tokens / (e2e_ms / 1000.0), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "host_buffers": {"thp": "page-locked transparent huge pages",
+                                 "torch": "torch pinned allocator"}[args.host_alloc]},
             "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
             "selection_quality": quality}
 

@@ -90,10 +90,8 @@ def load(path=None):
     L.msa_status_string.argtypes = [ci]
     L.msa_status_string.restype = ctypes.c_char_p
     for f in ("msa_index_topk", "msa_sparse_attn", "msa_forward", "msa_workspace_status",
-              "msa_index_topk_noalloc", "msa_debug_set_wait_polls", "msa_quality_workspace_bytes",
-           "msa_selection_quality", "msa_cache_append", "msa_forward_paged",
-           "msa_dense_workspace_bytes", "msa_dense_attn", "msa_index_kl_workspace_bytes",
-           "msa_index_kl"):
+              "msa_index_topk_noalloc", "msa_selection_quality", "msa_cache_append",
+              "msa_forward_paged", "msa_dense_attn", "msa_index_kl"):
         getattr(L, f).restype = ci
     if path == _build.LIBMSA:
         _lib = L

@@ -227,3 +227,17 @@ def test_dense_entry_point_validates_on_the_host(lib):
     kl1 = (ctypes.c_int32 * 1)(64)
     n1 = msa.msa_dense_workspace_bytes(p1)
     assert f(ctypes.byref(p1), a, a, a, qs1, kl1, a, a, n1 - 1, None) == WORKSPACE
+
+
+def test_workspace_sizes_above_two_gigabytes_come_back_whole(lib):
+    # every *_workspace_bytes call returns size_t: a 32K dense call needs
+    # about 2.5 GB, more than a 32-bit return could hold
+    p = msa.params(1, 32768, 48, 8, 128, 64, 256)
+    n = msa.msa_dense_workspace_bytes(p)
+    assert n > (1 << 31)
+    assert n >= 32768 * 48 * 128 * 4                   # the fp32 output accumulators alone
+    for f in (msa.msa_workspace_bytes, msa.msa_quality_workspace_bytes,
+              msa.msa_index_kl_workspace_bytes, msa.msa_dense_workspace_bytes):
+        assert f(p) > 0
+    big = msa.params(256, 1, 48, 8, 128, 64, 32768)    # 256 decode rows at 4M: quality scratch
+    assert msa.msa_quality_workspace_bytes(big) > (1 << 31)
