@@ -4,8 +4,8 @@
 One step = the whole hot path (index scoring, block max-pooling, top-16 with
 the local block forced, sparse softmax attention) over one batch of seeded
 synthetic inputs already resident in HBM.  The default line is the 1M-token
-chunked prefill, with the 64 x 256K decode batch measured in the same run and
-reported under "decode":
+chunked prefill, with the 128K single-call prefill and the 64 x 256K decode
+batch measured in the same run and nested under "prefill_128k" and "decode":
 
   decode_256k   64 sequences x 262144-token block-major caches, 1 new query
                 each (48 query / 8 KV heads, D 128, Di 64)
@@ -14,6 +14,10 @@ reported under "decode":
   prefill_32k   one 32768-token sequence
   decode_small  8 x 131072 decode (a small case for profiler captures)
   prefill_1m_last_chunk  the last 8192-query chunk of prefill_1m alone (profiling)
+  dense_32k     dense causal attention over a 32768-token prefill (msa_dense_attn)
+  decode_256k_paged  the decode batch from paged pools: the newest token of
+                each sequence appended through a shuffled block table
+                (msa_cache_append), then msa_forward_paged
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle (the
 reference arm) on a bounded sample of the same workload instead.

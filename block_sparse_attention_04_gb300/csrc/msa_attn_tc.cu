@@ -58,6 +58,12 @@ struct AttnPass {
   uint32_t wait_polls;   // poll cap of the pipeline waits (0: wall-clock bound only)
 };
 
+// Lists are ordered group-major, (g, b, kb): the tiles of one KV group are
+// contiguous, so CTAs dealt nearby tiles all work on one group at a time.
+__device__ __forceinline__ size_t list_of(const AttnPass& a, int b, int kb, int g) {
+  return ((size_t)g * a.s.B + b) * a.nbl + kb;
+}
+
 __device__ __forceinline__ bool slot_valid(const AttnPass& a, int b, int i, int kb) {
   const int64_t t = (int64_t)a.pos.q_start[b] + i;
   return kb >= 0 && kb <= (int)(t / kBlock) && kb < a.s.max_blocks;
@@ -79,7 +85,7 @@ __global__ void csr_count_kernel(AttnPass a) {
       flag_invalid(a.status);
       continue;
     }
-    atomicAdd(&a.count[((size_t)b * a.nbl + kb) * a.s.G + g], 1);
+    atomicAdd(&a.count[list_of(a, b, kb, g)], 1);
   }
 }
 
@@ -154,7 +160,7 @@ __global__ void csr_fill_kernel(AttnPass a) {
     const int b = (int)(r / a.Tp), il = (int)(r % a.Tp);
     const int kb = a.sel[(((size_t)b * a.s.T + a.t0 + il) * a.s.G + g) * kTopk + j];
     if (!slot_valid(a, b, a.t0 + il, kb)) continue;
-    const int L = (b * a.nbl + kb) * a.s.G + g;
+    const int L = (int)list_of(a, b, kb, g);
     const int p = atomicAdd(&a.cursor[L], 1);
     a.entries[a.off[L] + p] = il * kTopk + j;
   }
@@ -164,7 +170,7 @@ __global__ void csr_fill_kernel(AttnPass a) {
        L += (int64_t)gridDim.x * blockDim.x) {
     const int t0 = a.tile_off[L], t1 = a.tile_off[L + 1];
     if (t0 == t1) continue;
-    const int g = (int)(L % a.s.G), kb = (int)((L / a.s.G) % a.nbl), b = (int)(L / (a.s.G * a.nbl));
+    const int kb = (int)(L % a.nbl), b = (int)((L / a.nbl) % a.s.B), g = (int)(L / ((int64_t)a.nbl * a.s.B));
     const int cnt = a.count[L], o = a.off[L];
     for (int k = t0; k < t1; ++k) {
       const int e0 = (k - t0) * a.R;
@@ -174,6 +180,16 @@ __global__ void csr_fill_kernel(AttnPass a) {
 }
 
 // ---- the attention tile kernel ---------------------------------------------
+constexpr int kTileChunk = 4;   // consecutive tiles dealt to a CTA at a time
+
+// Local tile i of this CTA -> its descriptor (see the chunked deal in
+// attn_tc_kernel).
+struct CtaTiles {
+  const int4* all;
+  __device__ __forceinline__ int4 operator[](int i) const {
+    return all[((i / kTileChunk) * (int)gridDim.x + (int)blockIdx.x) * kTileChunk + i % kTileChunk];
+  }
+};
 constexpr int kQStages = 3;   // Q tiles in flight (the Q copy is the longest latency)
 constexpr int kKVStages = 2;  // K and V blocks in flight
 
@@ -247,13 +263,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   const int H = a.s.H, hpg = H / a.s.G;
   const int rshift = a.rpe == 8 ? 3 : 4;  // tile row -> entry
-  // a contiguous range of tiles per CTA: consecutive tiles of one list share
-  // the K/V block in shared memory
+  // This CTA's tiles: chunks of kTileChunk consecutive tiles (mostly of one
+  // list, so the K/V block in shared memory is reused within a chunk), dealt
+  // round-robin.  With group-major lists, all CTAs then work within a narrow
+  // stretch of the tile order, i.e. on one KV group at a time, whose Q rows
+  // and K/V blocks stay in L2; contiguous ranges per CTA had every CTA on a
+  // different group, and each query's Q rows were fetched from DRAM for
+  // most of its 16 blocks.
   const int ntiles = a.tile_off[a.nlists];
-  const int per = (ntiles + gridDim.x - 1) / gridDim.x;
-  const int tile_lo = blockIdx.x * per;
-  const int n = max(0, min(ntiles, tile_lo + per) - tile_lo);  // tiles of this CTA
-  const int4* desc = a.tile_desc + tile_lo;
+  const int nchunks = (ntiles + kTileChunk - 1) / kTileChunk;
+  const int my_chunks =
+      (int)blockIdx.x < nchunks ? (nchunks - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  int n = my_chunks * kTileChunk;                          // tiles of this CTA
+  if (my_chunks > 0 && (nchunks - 1) % (int)gridDim.x == (int)blockIdx.x)
+    n -= nchunks * kTileChunk - ntiles;                    // it holds the partial last chunk
+  const CtaTiles desc{a.tile_desc};
 
   if (warp == kQWarp) {
     // ---------------------------------------------------- Q TMA (warp 0)
