@@ -9,15 +9,18 @@
 //                 accumulation, block maxima kept in registers/shared memory.
 //   topk_merge    step 3: merges the per-split lists, forces the local block
 //                 in, sorts ids ascending, pads with -1.
-//   attn_stream   step 4 for one selected block of one (query, group): scores
-//                 of all heads of the group (mma), block-local softmax
-//                 statistics, P.V (mma), written as an unnormalised partial.
-//   attn_merge    combines the <= 16 block partials of each (query, head)
+//   attn_dec      step 4: a persistent CTA per SM; whole selected K/V blocks
+//                 of one KV head arrive by TMA through a ring of shared-memory
+//                 stages, and an online softmax over a part of a (query,
+//                 group)'s selected blocks (scores of all heads of the group
+//                 and P.V by mma) leaves one unnormalised partial per part.
+//   attn_merge    combines the parts' partials of each (query, head)
 //                 (log-sum-exp merge) into the bf16 output.
 #include <cfloat>
 #include <climits>
 
 #include "msa_device.cuh"
+#include "msa_tma.h"
 
 namespace msa {
 namespace {
@@ -92,24 +95,32 @@ __global__ void __launch_bounds__(kIdxWarps * 32) index_stream_kernel(
   const int nbw = (blk1 - blk0 - warp + kIdxWarps - 1) / kIdxWarps;
   const int n = nbw > 0 ? nbw * SPB : 0;
   uint4 C0[NU], C1[NU];  // rows gq and gq + 8 of the current step
-  // (a block-table entry outside the pool is flagged and block 0 read instead)
-#define MSA_IDX_LOAD(IT, X0, X1)                                                        \
-  do {                                                                                  \
-    const int blk_ = blk0 + warp + ((IT) / SPB) * kIdxWarps;                            \
-    const int64_t pb_ = cache_block(s, b, blk_, status);                                \
-    const uint16_t* r_ =                                                                \
-        k_idx + ((size_t)(pb_ < 0 ? 0 : pb_) * kBlock + ((IT) % SPB) * 16 + gq) * DI;    \
-    _Pragma("unroll") for (int u_ = 0; u_ < NU; ++u_) {                                 \
-      X0[u_] = ldg_stream(r_ + (tq + 4 * u_) * 8);                                      \
-      X1[u_] = ldg_stream(r_ + 8 * DI + (tq + 4 * u_) * 8);                             \
-    }                                                                                   \
+  // Row gq of the k-th block of this warp, resolved once per block (a
+  // block-table entry outside the pool is flagged and block 0 read instead).
+  const uint16_t* lrow = k_idx;
+#define MSA_IDX_BLOCK(K)                                                                  \
+  do {                                                                                    \
+    const int64_t pb_ = cache_block(s, b, blk0 + warp + (K) * kIdxWarps, status);         \
+    lrow = k_idx + ((size_t)(pb_ < 0 ? 0 : pb_) * kBlock + gq) * DI;                      \
   } while (0)
-  if (n > 0) MSA_IDX_LOAD(0, C0, C1);
+#define MSA_IDX_LOAD(STEP, X0, X1)                                                        \
+  do {                                                                                    \
+    const uint16_t* r_ = lrow + (STEP) * 16 * DI;                                         \
+    _Pragma("unroll") for (int u_ = 0; u_ < NU; ++u_) {                                   \
+      X0[u_] = ldg_stream(r_ + (tq + 4 * u_) * 8);                                        \
+      X1[u_] = ldg_stream(r_ + 8 * DI + (tq + 4 * u_) * 8);                               \
+    }                                                                                     \
+  } while (0)
+  if (n > 0) {
+    MSA_IDX_BLOCK(0);
+    MSA_IDX_LOAD(0, C0, C1);
+  }
   float m0 = -INFINITY, m1 = -INFINITY;
   for (int it = 0; it < n; ++it) {
     uint4 N0[NU], N1[NU];
     if (it + 1 < n) {
-      MSA_IDX_LOAD(it + 1, N0, N1);
+      if ((it + 1) % SPB == 0) MSA_IDX_BLOCK((it + 1) / SPB);
+      MSA_IDX_LOAD((it + 1) % SPB, N0, N1);
     } else {
 #pragma unroll
       for (int u = 0; u < NU; ++u) N0[u] = N1[u] = make_uint4(0, 0, 0, 0);
@@ -145,6 +156,7 @@ __global__ void __launch_bounds__(kIdxWarps * 32) index_stream_kernel(
     }
   }
 #undef MSA_IDX_LOAD
+#undef MSA_IDX_BLOCK
   __syncthreads();
 
   // Partial top-15 of this split, one warp per group, best first.
@@ -263,233 +275,375 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// attn_stream: grid (16 slots, G, pass rows); 128 threads (4 warps).
-// NTH = 8-head column tiles per group (heads per group <= 8 * NTH).
-template <int D, int NTH>
-__global__ void __launch_bounds__(128) attn_stream_kernel(
-    Shape s, Positions pos, int T, int t0, int Tp, const uint16_t* __restrict__ q,
-    const uint16_t* __restrict__ kc, const uint16_t* __restrict__ vc,
-    const int32_t* __restrict__ sel, float* __restrict__ part_o, float* __restrict__ part_ml,
-    int* __restrict__ status) {
-  constexpr int NJ = D / 16;          // k-steps of the score mma
-  constexpr int NU = D / 32;          // 16-byte loads per K row and thread
-  constexpr int VSTR = D + 8;         // padded V row (elements)
-  constexpr int PSTR = kBlock + 8;    // padded P row (elements)
-  constexpr int NH = NTH * 8;
-  __shared__ __align__(16) uint16_t vs[kBlock * VSTR];
-  __shared__ __align__(16) uint16_t ps[NH * PSTR];
-  __shared__ float red[4][NH];
+// attn_dec: a persistent CTA per SM walks work items (pass row, group, part);
+// a part is spp = 16 / nparts consecutive selection slots.  Warp 4 (one lane)
+// reads the part's selected ids, resolves each to its cache block and copies
+// the block's K and V (128 tokens x D of one KV head, two 3-D TMA boxes of 64
+// dims each) into a ring of stages, and the group's query rows into one of
+// two query buffers by a bulk copy, running ahead of the compute by the depth
+// of the ring.  Warps 0-3 run an online softmax over the part's blocks:
+// S^T = K Q^T (tokens x heads) and O^T += V^T P^T with mma.sync, operands
+// read from the 128-byte-swizzled stages with ldmatrix; then one unnormalised
+// partial (O relative to the running max m, and m, l) per (row, head, part).
+struct DecArgs {
+  Shape s;
+  Positions pos;
+  int T, t0, Tp, nparts, spp, nitems;
+  const uint16_t* q;
+  const int32_t* sel;
+  float* part_o;
+  float* part_ml;
+  int* status;
+  uint32_t wait_polls;
+};
 
-  const int slot = blockIdx.x, g = blockIdx.y, row = blockIdx.z;
-  const int b = row / Tp, i = t0 + row % Tp;
-  const int64_t t = (int64_t)pos.q_start[b] + i;
-  const int lb = (int)(t / kBlock);
+constexpr int kDecConsumers = 128;          // warps 0-3
+constexpr int kDecThreads = kDecConsumers + 32;
+
+template <int D, int NTH>
+struct DecCfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kBox = 64 * kBlock * 2;                // one 64-dim box, 16 KiB
+  static constexpr int kStageBytes = 2 * kHalves * kBox;      // K boxes, then V boxes
+  static constexpr int kStages = D == 128 ? 3 : 6;            // 192 KiB of blocks in flight
+  static constexpr int NH = NTH * 8;
+  static constexpr int PSTR = kBlock + 8;                     // padded P row (elements)
+  static constexpr int kQBytes = NH * D * 2;
+  static constexpr int kQBufs = 4;                            // query buffers (items ahead)
+  static constexpr int kStagesOff = 0;
+  static constexpr int kQOff = kStages * kStageBytes;
+  static constexpr int kPOff = kQOff + kQBufs * kQBytes;
+  static constexpr int kRedOff = kPOff + NH * PSTR * 2;       // [2][4][NH] float
+  static constexpr int kLsumOff = kRedOff + 2 * 4 * NH * 4;   // [2][4][NH] float
+  static constexpr int kMetaOff = kLsumOff + 2 * 4 * NH * 4;  // [kStages] int
+  static constexpr int kBarOff = (kMetaOff + kStages * 4 + 7) / 8 * 8;
+  static constexpr int kBytes = kBarOff + (2 * kStages + 2 * kQBufs) * 8;
+  static constexpr int kSmem = kBytes + 1024;                 // base alignment slack
+};
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a box written
+// with the 128-byte swizzle (rows of 128 bytes, chunk index xor row % 8).
+__device__ __forceinline__ uint32_t swz128(int row, int chunk) {
+  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+template <int D, int NTH>
+__global__ void __launch_bounds__(kDecThreads, 1) attn_dec_kernel(
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    const __grid_constant__ DecArgs a) {
+  using C = DecCfg<D, NTH>;
+  constexpr int NJ = D / 16;     // k-steps of the score mma
+  constexpr int MGV = D / 64;    // 16-dim groups of O per warp
+  constexpr int NH = C::NH;
+  constexpr int S = C::kStages;
+  constexpr int NQ = C::kQBufs;
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint16_t* qbuf = reinterpret_cast<uint16_t*>(sm + C::kQOff);
+  uint16_t* ps = reinterpret_cast<uint16_t*>(sm + C::kPOff);
+  float* red = reinterpret_cast<float*>(sm + C::kRedOff);
+  float* lsum = reinterpret_cast<float*>(sm + C::kLsumOff);
+  int* meta_kb = reinterpret_cast<int*>(sm + C::kMetaOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+  uint64_t* empty = full + S;
+  uint64_t* q_full = empty + S;
+  uint64_t* q_empty = q_full + NQ;
+
+  const Shape& s = a.s;
   const int H = s.H, G = s.G, hpg = H / G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = lane >> 2, tq = lane & 3;
-  const size_t ml_base = ((size_t)row * H + (size_t)g * hpg) * kTopk + slot;
 
-  // Q^T fragments (dims x heads), same dim permutation as the K fragments;
-  // loaded before the selection so that the two loads overlap
-  uint32_t bq[NTH][NJ][2];
-#pragma unroll
-  for (int nt = 0; nt < NTH; ++nt) {
-    const int hh = nt * 8 + gq;
-    const uint16_t* qr = q + ((size_t)(b * T + i) * H + (size_t)g * hpg + (hh < hpg ? hh : 0)) * D;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      const int base = (tq + 4 * (j >> 1)) * 8 + (j & 1) * 4;
-      uint32_t lo = *reinterpret_cast<const uint32_t*>(qr + base);
-      uint32_t hi = *reinterpret_cast<const uint32_t*>(qr + base + 2);
-      bq[nt][j][0] = hh < hpg ? lo : 0u;
-      bq[nt][j][1] = hh < hpg ? hi : 0u;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 4);
     }
+    for (int i = 0; i < NQ; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 4);
+    }
+    fence_mbar_init();
   }
+  // query rows past the group's heads stay zero (their columns are computed
+  // and never written)
+  for (int e = threadIdx.x; e < NQ * NH * D / 2; e += blockDim.x) {
+    const int r = (e * 2 / D) % NH;
+    if (r >= hpg) reinterpret_cast<uint32_t*>(qbuf)[e] = 0u;
+  }
+  __syncthreads();
 
-  int kb = sel[((size_t)(b * T + i) * G + g) * kTopk + slot];
-  if (kb > lb || kb >= s.max_blocks) {
-    if (threadIdx.x == 0) flag_invalid(status);
-    kb = -1;
-  }
-  int64_t pb = -1;   // the cache block holding it
-  if (kb >= 0) {
-    pb = cache_block(s, b, kb, nullptr);
-    if (pb < 0) {
-      if (threadIdx.x == 0) flag_invalid(status);
-      kb = -1;
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      const uint32_t qbytes = (uint32_t)(hpg * D * 2);
+      int n = 0, k = 0, nq = 0;   // stages armed, items begun, query copies issued
+      bool ok = true;
+      for (int item = blockIdx.x; item < a.nitems && ok; item += gridDim.x, ++k) {
+        const int unit = item / a.nparts, part = item % a.nparts;
+        const int row = unit / G, g = unit % G;
+        const int b = row / a.Tp, i = a.t0 + row % a.Tp;
+        const int64_t t = (int64_t)a.pos.q_start[b] + i;
+        const int lb = (int)(t / kBlock);
+        const int qs = k % NQ;
+        if (k >= NQ && !mbar_wait(&q_empty[qs], ((k / NQ) - 1) & 1, a.status, a.wait_polls)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&q_full[qs], qbytes);
+        bulk_load(smem_u32(qbuf + qs * NH * D),
+                  a.q + ((size_t)(b * a.T + i) * H + (size_t)g * hpg) * D, qbytes, &q_full[qs]);
+        ++nq;
+        const int32_t* srow = a.sel + ((size_t)(b * a.T + i) * G + g) * kTopk + part * a.spp;
+        for (int j = 0; j < a.spp; ++j, ++n) {
+          int kb = srow[j];
+          if (kb > lb || kb >= s.max_blocks) {
+            flag_invalid(a.status);
+            kb = -1;
+          }
+          int64_t pb = -1;
+          if (kb >= 0) {
+            pb = cache_block(s, b, kb, a.status);
+            if (pb < 0) kb = -1;
+          }
+          const int st = n % S;
+          if (n >= S && !mbar_wait(&empty[st], ((n / S) - 1) & 1, a.status, a.wait_polls)) {
+            ok = false;
+            break;
+          }
+          meta_kb[st] = kb;
+          if (kb < 0) {
+            mbar_arrive(&full[st]);
+            continue;
+          }
+          mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+          const uint32_t kdst = smem_u32(sm + C::kStagesOff + st * C::kStageBytes);
+          const uint32_t vdst = kdst + C::kHalves * C::kBox;
+          const int z = (int)(pb * kBlock);
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h) {
+            tma_load_3d_hint(kdst + h * C::kBox, &tm_k, &full[st], h * 64, g, z, pol);
+            tma_load_3d_hint(vdst + h * C::kBox, &tm_v, &full[st], h * 64, g, z, pol);
+          }
+        }
+      }
+      // Wait (wall clock only) for the last copies of every buffer, so that
+      // none lands after the CTA has exited, also when the consumers have
+      // given up or this lane stopped issuing after a wait ran out.
+      for (int m = n - 1; m >= 0 && m >= n - S; --m) mbar_wait(&full[m % S], (m / S) & 1, nullptr);
+      for (int m = nq - 1; m >= 0 && m >= nq - NQ; --m)
+        mbar_wait(&q_full[m % NQ], (m / NQ) & 1, nullptr);
     }
-  }
-  if (kb < 0) {
-    for (int h = threadIdx.x; h < hpg; h += blockDim.x) {
-      part_ml[(ml_base + (size_t)h * kTopk) * 2 + 0] = -INFINITY;
-      part_ml[(ml_base + (size_t)h * kTopk) * 2 + 1] = 0.f;
-    }
+    __syncwarp();
     return;
   }
 
-  const size_t tok_stride = (size_t)G * D;
-  const uint16_t* kblk = kc + (size_t)pb * kBlock * tok_stride + (size_t)g * D;
-  const uint16_t* vblk = vc + (size_t)pb * kBlock * tok_stride + (size_t)g * D;
-
-  // scores S^T[token][head] for this warp's 32 tokens
-  float sc[2][NTH][4];
+  // -------------------------------------------------------------- consumers
+  const int gq = lane >> 2, tq = lane & 3;
   const float qk_scale = s.scale * kLog2e;
-  // the warp's whole 32-token K slice is requested before the first score MMA
-  // and before the V copy, which is needed later: twice the bytes in flight of
-  // loading K in 16-token halves, and K first in the memory queue (measured
-  // 0.128 -> 0.101 ms on the 64 x 256K decode batch, although the registers
-  // this holds leave 4 CTAs per SM instead of 6)
-  uint4 LL0[2][NU], LL1[2][NU];
-#pragma unroll
-  for (int mg = 0; mg < 2; ++mg) {
-    const uint16_t* k0 = kblk + (size_t)(warp * 32 + mg * 16 + gq) * tok_stride;
-    const uint16_t* k1 = k0 + 8 * tok_stride;
-#pragma unroll
-    for (int u = 0; u < NU; ++u) {
-      LL0[mg][u] = ldg_stream(k0 + (tq + 4 * u) * 8);
-      LL1[mg][u] = ldg_stream(k1 + (tq + 4 * u) * 8);
-    }
-  }
-  // V block -> shared memory (lands during the score computation)
-  for (int c = threadIdx.x; c < kBlock * (D / 8); c += blockDim.x) {
-    const int r = c / (D / 8), ch = c % (D / 8);
-    cp_async_16(smem_u32(vs + r * VSTR + ch * 8), vblk + r * tok_stride + ch * 8);
-  }
-  cp_async_commit();
+  int n = 0, vb = 0, k = 0;
+  for (int item = blockIdx.x; item < a.nitems; item += gridDim.x, ++k) {
+    const int unit = item / a.nparts, part = item % a.nparts;
+    const int row = unit / G, g = unit % G;
+    const int b = row / a.Tp, i = a.t0 + row % a.Tp;
+    const int64_t t = (int64_t)a.pos.q_start[b] + i;
+    const int lb = (int)(t / kBlock);
+    const int qs = k % NQ;
 
+    bool ok = mbar_wait(&q_full[qs], (k / NQ) & 1, a.status, a.wait_polls);
+    if (!named_bar_and(1, kDecConsumers, ok)) return;
+    // Q^T fragments (dims x heads) of this item
+    uint32_t bq[NTH][NJ][2];
+    {
+      const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qbuf + qs * NH * D);
 #pragma unroll
-  for (int mg = 0; mg < 2; ++mg) {
-    const int r0 = warp * 32 + mg * 16 + gq;
-    const uint4* L0 = LL0[mg];
-    const uint4* L1 = LL1[mg];
+      for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
-    for (int nt = 0; nt < NTH; ++nt) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        const int u = j >> 1;
-        const bool e = j & 1;
-        mma_bf16_16816(acc, e ? L0[u].z : L0[u].x, e ? L1[u].z : L1[u].x,
-                       e ? L0[u].w : L0[u].y, e ? L1[u].w : L1[u].y, bq[nt][j][0],
-                       bq[nt][j][1]);
-      }
-      const int64_t tok0 = (int64_t)kb * kBlock + r0;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int64_t tok = tok0 + (c >= 2 ? 8 : 0);
-        sc[mg][nt][c] = tok <= t ? acc[c] * qk_scale : -INFINITY;
-      }
-    }
-  }
-
-  // block-local max per head
-  float mh[NTH][2];
-#pragma unroll
-  for (int nt = 0; nt < NTH; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float m = fmaxf(fmaxf(sc[0][nt][e], sc[0][nt][e + 2]), fmaxf(sc[1][nt][e], sc[1][nt][e + 2]));
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (gq == 0) red[warp][nt * 8 + 2 * tq + e] = m;
-    }
-  __syncthreads();
-#pragma unroll
-  for (int nt = 0; nt < NTH; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int h = nt * 8 + 2 * tq + e;
-      mh[nt][e] = fmaxf(fmaxf(red[0][h], red[1][h]), fmaxf(red[2][h], red[3][h]));
-    }
-  __syncthreads();
-
-  // p = 2^(s - m) -> bf16 P[head][token]; row sums
-  float lh[NTH][2];
-#pragma unroll
-  for (int nt = 0; nt < NTH; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int h = nt * 8 + 2 * tq + e;
-      float sum = 0.f;
-#pragma unroll
-      for (int mg = 0; mg < 2; ++mg)
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const float p = ex2(sc[mg][nt][e + 2 * rr] - mh[nt][e]);
-          sum += p;
-          ps[h * PSTR + warp * 32 + mg * 16 + gq + 8 * rr] = (uint16_t)f32_to_bf16_rne(p);
+        for (int j = 0; j < NJ; ++j) {
+          const int w0 = ((nt * 8 + gq) * D + j * 16 + 2 * tq) / 2;
+          bq[nt][j][0] = q32[w0];
+          bq[nt][j][1] = q32[w0 + 4];
         }
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      lh[nt][e] = sum;
-      if (gq == 0) red[warp][h] = sum;
     }
-  cp_async_wait<0>();
-  __syncthreads();
 
-  // O^T[dim][head] = V^T P^T; warp w owns dims [w*D/4, (w+1)*D/4)
-  constexpr int MGV = D / 64;  // 16-dim groups per warp
-  float o[MGV][NTH][4];
-#pragma unroll
-  for (int mg = 0; mg < MGV; ++mg)
-#pragma unroll
-    for (int nt = 0; nt < NTH; ++nt)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) o[mg][nt][c] = 0.f;
-  const uint32_t* p32 = reinterpret_cast<const uint32_t*>(ps);
-#pragma unroll
-  for (int ks = 0; ks < kBlock / 16; ++ks) {
-#pragma unroll
-    for (int mg = 0; mg < MGV; ++mg) {
-      const int dim0 = warp * (D / 4) + mg * 16;
-      const int mi = lane >> 3;
-      const int tok = ks * 16 + (lane & 7) + ((mi & 2) ? 8 : 0);
-      const int dim = dim0 + ((mi & 1) ? 8 : 0);
-      uint32_t a[4];
-      ldmatrix_x4_trans(a, smem_u32(vs + tok * VSTR + dim));
-#pragma unroll
-      for (int nt = 0; nt < NTH; ++nt) {
-        const int h = nt * 8 + gq;
-        const uint32_t b0 = p32[(h * PSTR) / 2 + ks * 8 + tq];
-        const uint32_t b1 = p32[(h * PSTR) / 2 + ks * 8 + 4 + tq];
-        mma_bf16_16816(o[mg][nt], a[0], a[1], a[2], a[3], b0, b1);
-      }
-    }
-  }
-
-  // partial outputs (unnormalised, relative to the block max)
-#pragma unroll
-  for (int mg = 0; mg < MGV; ++mg)
-#pragma unroll
-    for (int nt = 0; nt < NTH; ++nt)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int h = nt * 8 + 2 * tq + (c & 1);
-        const int dim = warp * (D / 4) + mg * 16 + gq + (c >= 2 ? 8 : 0);
-        if (h < hpg) part_o[(ml_base + (size_t)h * kTopk) * D + dim] = o[mg][nt][c];
-      }
-  if (threadIdx.x < 32) {
+    float o[MGV][NTH][4];
+    float m_run[NTH][2], l_w[NTH][2];
 #pragma unroll
     for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int h = nt * 8 + 2 * tq + e;
-        const float l = red[0][h] + red[1][h] + red[2][h] + red[3][h];
-        if (gq == 0 && h < hpg) {
-          part_ml[(ml_base + (size_t)h * kTopk) * 2 + 0] = mh[nt][e];
-          part_ml[(ml_base + (size_t)h * kTopk) * 2 + 1] = l;
-        }
+        m_run[nt][e] = -INFINITY;
+        l_w[nt][e] = 0.f;
       }
+#pragma unroll
+    for (int mg = 0; mg < MGV; ++mg)
+#pragma unroll
+      for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[mg][nt][c] = 0.f;
+
+    for (int j = 0; j < a.spp; ++j, ++n) {
+      const int st = n % S;
+      ok = mbar_wait(&full[st], (n / S) & 1, a.status, a.wait_polls);
+      if (!named_bar_and(1, kDecConsumers, ok)) return;
+      const int kb = meta_kb[st];
+      if (kb >= 0) {
+        const uint32_t kbase = smem_u32(sm + C::kStagesOff + st * C::kStageBytes);
+        const uint32_t vbase = kbase + C::kHalves * C::kBox;
+        // scores S^T[token][head] of this warp's 32 tokens
+        float sc[2][NTH][4];
+#pragma unroll
+        for (int mg = 0; mg < 2; ++mg) {
+          const int tok = warp * 32 + mg * 16 + (lane & 15);
+#pragma unroll
+          for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sc[mg][nt][c] = 0.f;
+#pragma unroll
+          for (int jj = 0; jj < NJ; ++jj) {
+            uint32_t ka[4];
+            ldmatrix_x4(ka, kbase + (jj >> 2) * C::kBox +
+                                swz128(tok, (jj & 3) * 2 + (lane >> 4)));
+#pragma unroll
+            for (int nt = 0; nt < NTH; ++nt)
+              mma_bf16_16816(sc[mg][nt], ka[0], ka[1], ka[2], ka[3], bq[nt][jj][0],
+                             bq[nt][jj][1]);
+          }
+          const int64_t tok0 = (int64_t)kb * kBlock + warp * 32 + mg * 16 + gq;
+#pragma unroll
+          for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              sc[mg][nt][c] = (kb < lb || tok0 + (c >= 2 ? 8 : 0) <= t)
+                                  ? sc[mg][nt][c] * qk_scale
+                                  : -INFINITY;
+        }
+        // block max per head over the four warps, new running max
+        float* rd = red + (vb & 1) * 4 * NH;
+#pragma unroll
+        for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float m = fmaxf(fmaxf(sc[0][nt][e], sc[0][nt][e + 2]),
+                            fmaxf(sc[1][nt][e], sc[1][nt][e + 2]));
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1)
+              m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if (gq == 0) rd[warp * NH + nt * 8 + 2 * tq + e] = m;
+          }
+        named_bar_sync(1, kDecConsumers);
+        float alpha[NTH][2];
+#pragma unroll
+        for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int h = nt * 8 + 2 * tq + e;
+            const float bm = fmaxf(fmaxf(rd[h], rd[NH + h]), fmaxf(rd[2 * NH + h], rd[3 * NH + h]));
+            const float mn = fmaxf(m_run[nt][e], bm);
+            alpha[nt][e] = ex2(m_run[nt][e] - mn);
+            m_run[nt][e] = mn;
+          }
+        // p = 2^(s - m) -> bf16 P[head][token]; this warp's row sums
+#pragma unroll
+        for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int h = nt * 8 + 2 * tq + e;
+            float sum = 0.f;
+#pragma unroll
+            for (int mg = 0; mg < 2; ++mg)
+#pragma unroll
+              for (int rr = 0; rr < 2; ++rr) {
+                const float p = ex2(sc[mg][nt][e + 2 * rr] - m_run[nt][e]);
+                sum += p;
+                ps[h * C::PSTR + warp * 32 + mg * 16 + gq + 8 * rr] =
+                    (uint16_t)f32_to_bf16_rne(p);
+              }
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            l_w[nt][e] = l_w[nt][e] * alpha[nt][e] + sum;
+          }
+#pragma unroll
+        for (int mg = 0; mg < MGV; ++mg)
+#pragma unroll
+          for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) o[mg][nt][c] *= alpha[nt][c & 1];
+        named_bar_sync(1, kDecConsumers);
+        // O^T[dim][head] += V^T P^T; warp w owns dims [w*D/4, (w+1)*D/4)
+        const uint32_t* p32 = reinterpret_cast<const uint32_t*>(ps);
+#pragma unroll
+        for (int ks = 0; ks < kBlock / 16; ++ks) {
+#pragma unroll
+          for (int mg = 0; mg < MGV; ++mg) {
+            const int mi = lane >> 3;
+            const int tok = ks * 16 + (lane & 7) + ((mi & 2) ? 8 : 0);
+            const int dim = warp * (D / 4) + mg * 16 + ((mi & 1) ? 8 : 0);
+            uint32_t va[4];
+            ldmatrix_x4_trans(va, vbase + (dim >> 6) * C::kBox + swz128(tok, (dim & 63) >> 3));
+#pragma unroll
+            for (int nt = 0; nt < NTH; ++nt) {
+              const int h = nt * 8 + gq;
+              const uint32_t b0 = p32[(h * C::PSTR) / 2 + ks * 8 + tq];
+              const uint32_t b1 = p32[(h * C::PSTR) / 2 + ks * 8 + 4 + tq];
+              mma_bf16_16816(o[mg][nt], va[0], va[1], va[2], va[3], b0, b1);
+            }
+          }
+        }
+        ++vb;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    // The query buffer goes back only now: the score MMAs have consumed the
+    // fragments, so no load of them can still be outstanding when the next
+    // copy overwrites the buffer.
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&q_empty[qs]);
+
+    // the item's partials: O relative to m, and (m, l) per head
+    float* ls = lsum + (k & 1) * 4 * NH;
+    if (gq == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) ls[warp * NH + nt * 8 + 2 * tq + e] = l_w[nt][e];
+    }
+    named_bar_sync(1, kDecConsumers);
+    const size_t hbase = ((size_t)row * H + (size_t)g * hpg) * a.nparts + part;
+#pragma unroll
+    for (int mg = 0; mg < MGV; ++mg)
+#pragma unroll
+      for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int h = nt * 8 + 2 * tq + (c & 1);
+          const int dim = warp * (D / 4) + mg * 16 + gq + (c >= 2 ? 8 : 0);
+          if (h < hpg) a.part_o[(hbase + (size_t)h * a.nparts) * D + dim] = o[mg][nt][c];
+        }
+    if (warp == 0 && gq == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int h = nt * 8 + 2 * tq + e;
+          if (h < hpg) {
+            const float l = ls[h] + ls[NH + h] + ls[2 * NH + h] + ls[3 * NH + h];
+            a.part_ml[(hbase + (size_t)h * a.nparts) * 2 + 0] = m_run[nt][e];
+            a.part_ml[(hbase + (size_t)h * a.nparts) * 2 + 1] = l;
+          }
+        }
+    }
   }
-  (void)lh;
 }
 
 // ---------------------------------------------------------------------------
-// attn_merge: one warp per (pass row, head).
+// attn_merge: one warp per (pass row, head), over its nparts partials.
 // DENSE: fold into the dense accumulators instead (one chunk of msa_dense_attn).
 template <int D, bool DENSE>
 __global__ void __launch_bounds__(256) attn_merge_kernel(
-    Shape s, int T, int t0, int Tp, int nrows, const float* __restrict__ part_o,
+    Shape s, int T, int t0, int Tp, int nrows, int nparts, const float* __restrict__ part_o,
     const float* __restrict__ part_ml, uint16_t* __restrict__ out, DenseStep ds) {
   constexpr int PER = D / 32;
   const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -497,9 +651,9 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(
   if (gw >= nrows * s.H) return;
   const int row = gw / s.H, h = gw % s.H;
   const int b = row / Tp, i = t0 + row % Tp;
-  const size_t base = ((size_t)row * s.H + h) * kTopk;
+  const size_t base = ((size_t)row * s.H + h) * nparts;
   float m = -INFINITY, l = 0.f;
-  if (lane < kTopk) {
+  if (lane < nparts) {
     m = part_ml[(base + lane) * 2];
     l = part_ml[(base + lane) * 2 + 1];
   }
@@ -513,7 +667,7 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  for (int j = 0; j < kTopk; ++j) {
+  for (int j = 0; j < nparts; ++j) {
     const float wj = __shfl_sync(0xffffffffu, w, j);
     if (wj == 0.f) continue;
     const float* src = part_o + (base + j) * D + lane * PER;
@@ -695,6 +849,29 @@ cudaError_t launch_dense_sel(const Shape& s, const Positions& pos, int chunk, in
   return cudaGetLastError();
 }
 
+namespace {
+
+// Parts per (row, group) of the streaming attention: the fewest (of 1, 2, 4,
+// 8, 16) that give every CTA of the persistent grid a dozen work items or more.
+int attn_stream_parts(int units, int ctas) {
+  int p = 1;
+  while (p < kTopk && (int64_t)units * p < 12 * (int64_t)ctas) p *= 2;
+  return p;
+}
+
+template <int D, int NTH>
+cudaError_t launch_attn_dec(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const DecArgs& a,
+                            int grid, cudaStream_t st) {
+  using C = DecCfg<D, NTH>;
+  cudaError_t e = cudaFuncSetAttribute(attn_dec_kernel<D, NTH>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  attn_dec_kernel<D, NTH><<<grid, kDecThreads, C::kSmem, st>>>(tm_k, tm_v, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_attn_stream(const Shape& s, const Positions& pos, int t0, int t1,
                                const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                const int32_t* sel, uint16_t* out, const Workspace& ws,
@@ -703,26 +880,55 @@ cudaError_t launch_attn_stream(const Shape& s, const Positions& pos, int t0, int
   const int rows = s.B * Tp;
   if (rows <= 0) return cudaSuccess;
   const int hpg = s.H / s.G;
-  dim3 grid(kTopk, s.G, rows);
-  note_launches(2);
-#define MSA_ATTN_STREAM(DD, NT)                                                              \
-  attn_stream_kernel<DD, NT><<<grid, 128, 0, st>>>(s, pos, s.T, t0, Tp, q, k, v, sel,       \
-                                                   ws.part_o, ws.part_ml, ws.status)
-  if (s.D == 128) {
-    if (hpg <= 8) MSA_ATTN_STREAM(128, 1); else MSA_ATTN_STREAM(128, 2);
-  } else {
-    if (hpg <= 8) MSA_ATTN_STREAM(64, 1); else MSA_ATTN_STREAM(64, 2);
+  // K and V as (D dims, G heads, cache tokens); one box = 64 dims x 128
+  // tokens of one head, the 128-byte swizzle the consumers index
+  CUtensorMap tm_k, tm_v;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)s.D, (cuuint64_t)s.G, (cuuint64_t)(s.cache_blocks() * kBlock)};
+    cuuint64_t strides[2] = {(cuuint64_t)s.D * 2, (cuuint64_t)s.G * s.D * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)kBlock};
+    if (!encode_bf16_map(&tm_k, k, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_bf16_map(&tm_v, v, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
   }
-#undef MSA_ATTN_STREAM
+  const int ctas = sm_count();
+  const int units = rows * s.G;
+  DecArgs a;
+  a.s = s;
+  a.pos = pos;
+  a.T = s.T;
+  a.t0 = t0;
+  a.Tp = Tp;
+  a.nparts = attn_stream_parts(units, ctas);
+  a.spp = kTopk / a.nparts;
+  a.nitems = units * a.nparts;
+  a.q = q;
+  a.sel = sel;
+  a.part_o = ws.part_o;
+  a.part_ml = ws.part_ml;
+  a.status = ws.status;
+  a.wait_polls = debug_wait_polls();
+  const int grid = a.nitems < ctas ? a.nitems : ctas;
+  note_launches(2);
+  cudaError_t e;
+  if (s.D == 128)
+    e = hpg <= 8 ? launch_attn_dec<128, 1>(tm_k, tm_v, a, grid, st)
+                 : launch_attn_dec<128, 2>(tm_k, tm_v, a, grid, st);
+  else
+    e = hpg <= 8 ? launch_attn_dec<64, 1>(tm_k, tm_v, a, grid, st)
+                 : launch_attn_dec<64, 2>(tm_k, tm_v, a, grid, st);
+  if (e != cudaSuccess) return e;
   const int warps = rows * s.H;
   const DenseStep ds = dense ? *dense : DenseStep{};
-#define MSA_ATTN_MERGE(DD)                                                                       \
-  if (dense)                                                                                     \
-    attn_merge_kernel<DD, true><<<(warps + 7) / 8, 256, 0, st>>>(s, s.T, t0, Tp, rows, ws.part_o, \
-                                                                 ws.part_ml, out, ds);           \
-  else                                                                                           \
-    attn_merge_kernel<DD, false><<<(warps + 7) / 8, 256, 0, st>>>(s, s.T, t0, Tp, rows,          \
-                                                                  ws.part_o, ws.part_ml, out, ds)
+#define MSA_ATTN_MERGE(DD)                                                                      \
+  if (dense)                                                                                    \
+    attn_merge_kernel<DD, true><<<(warps + 7) / 8, 256, 0, st>>>(s, s.T, t0, Tp, rows,          \
+                                                                 a.nparts, ws.part_o,           \
+                                                                 ws.part_ml, out, ds);          \
+  else                                                                                          \
+    attn_merge_kernel<DD, false><<<(warps + 7) / 8, 256, 0, st>>>(s, s.T, t0, Tp, rows,         \
+                                                                  a.nparts, ws.part_o,          \
+                                                                  ws.part_ml, out, ds)
   if (s.D == 128) {
     MSA_ATTN_MERGE(128);
   } else {

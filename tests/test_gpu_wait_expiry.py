@@ -37,15 +37,25 @@ def _status(msa, ws):
         return e.status
 
 
-def test_pipeline_wait_expiry_is_reported_then_next_call_is_exact(msa, ref):
+# the tensor-core prefill kernels, and the streaming path's TMA-fed attention
+# on a decode batch (its index scan has no pipeline waits)
+CASES = {
+    "tensorcore": dict(B=1, T=3000, H=48, G=8, D=128, Di=64, ctx=[6000], q_start=[3000]),
+    "streaming": dict(B=6, T=1, H=48, G=8, D=128, Di=64, ctx=[9000, 4097, 128, 20000, 2500, 700],
+                      q_start=[8999, 4096, 127, 19999, 2499, 699]),
+}
+
+
+@pytest.mark.parametrize("kernels", sorted(CASES))
+def test_pipeline_wait_expiry_is_reported_then_next_call_is_exact(msa, ref, kernels):
     import torch
-    wl = Workload(B=1, T=3000, H=48, G=8, D=128, Di=64, ctx=[6000], q_start=[3000])
+    wl = Workload(**CASES[kernels])
     want_sel, want_out = wl.oracle(ref)
     dev = wl.device()
-    p = wl.params(msa, "tensorcore")
+    p = wl.params(msa, kernels)
     ws = msa.workspace(p)
-    sel = torch.full((1, wl.T, wl.G, 16), -7, dtype=torch.int32, device="cuda")
-    out = torch.zeros((1, wl.T, wl.H, wl.D), dtype=torch.int16, device="cuda")
+    sel = torch.full((wl.B, wl.T, wl.G, 16), -7, dtype=torch.int32, device="cuda")
+    out = torch.zeros((wl.B, wl.T, wl.H, wl.D), dtype=torch.int16, device="cuda")
     ref_sel = torch.from_numpy(want_sel).cuda()
 
     seen = {"index": [], "attn": []}
@@ -62,7 +72,8 @@ def test_pipeline_wait_expiry_is_reported_then_next_call_is_exact(msa, ref):
     torch.cuda.synchronize()          # the context is still usable
     for k, v in seen.items():
         assert set(v) <= {0, TIMEOUT}, (k, v)
-        assert TIMEOUT in v, ("no wait ran out", k, v)
+        if k == "attn" or kernels == "tensorcore":
+            assert TIMEOUT in v, ("no wait ran out", k, v)
 
     # the next calls on the same workspace: the status word is reset and the
     # results are exact again
