@@ -166,13 +166,14 @@ def quality(d, t, q_t, k_seq, sel_t, want_mass=False):
 def index_kl(d, t, q_idx_t, k_idx_seq, q_t, k_seq, sel_t, dk_idx=None):
     """One query's KL(P||Q) per group and its gradient (see msa_ref.h):
     returns (kl [G], dq_idx [G][Di]); dk_idx [>= t+1][Di] float64 is
-    accumulated into when given."""
+    accumulated into when given (by default a scratch array as long as
+    k_idx_seq, so that a write past token t stays inside it)."""
     q_idx_t, k_idx_seq, q_t, k_seq = _u16(q_idx_t), _u16(k_idx_seq), _u16(q_t), _u16(k_seq)
     sel_t = np.ascontiguousarray(sel_t, np.int32)
     kl = np.empty(d.G, np.float64)
     dq = np.empty((d.G, d.Di), np.float64)
     if dk_idx is None:
-        dk_idx = np.zeros((t + 1, d.Di), np.float64)
+        dk_idx = np.zeros((max(t + 1, k_idx_seq.shape[0]), d.Di), np.float64)
     assert dk_idx.dtype == np.float64 and dk_idx.flags.c_contiguous and dk_idx.shape[0] > t
     _check(lib().msa_ref_index_kl(ctypes.byref(d), t, _p(q_idx_t), _p(k_idx_seq), _p(q_t),
                                   _p(k_seq), _p(sel_t), _p(kl), _p(dq), _p(dk_idx)), "index_kl")

@@ -43,7 +43,7 @@ def test_single_candidate_gives_zero_loss_and_gradient(ref):
     for t in (0, 60, 127):
         sel = np.full((2, 16), -1, np.int32)
         sel[:, 0] = 0
-        dk = np.zeros((t + 1, 16))
+        dk = np.zeros((len(k_idx), 16))
         kl, dq = ref.index_kl(d, t, q_idx, k_idx, q, k, sel, dk)
         # P = Q = 1 up to the rounding of one softmax sum
         assert np.all(np.abs(kl) < 1e-13) and np.all(np.abs(dq) < 1e-13)
@@ -106,14 +106,16 @@ def test_gradients_match_finite_differences_of_the_loss(ref):
         fd = (ref.index_kl(d, t, qp, k_idx, q, k, sel)[0][g] -
               ref.index_kl(d, t, qm, k_idx, q, k, sel)[0][g]) / (2 * h)
         assert abs(fd - dq[g, dim]) < 1e-6 + 1e-3 * abs(dq[g, dim]), (g, dim, fd, dq[g, dim])
-    # dk: perturb one component of a token that is some block's maximum
-    dk = np.zeros((t + 1, Di))
+    # dk: perturb one component of a token that is some block's maximum; no
+    # gradient reaches a token after t (the pooled scores are causal)
+    dk = np.zeros((len(k_idx), Di))
     ref.index_kl(d, t, q_idx, k_idx, q, k, sel, dk)
+    assert np.all(dk[t + 1:] == 0)
     tok = int(np.argmax(np.abs(dk).sum(axis=1)))
     for dim in (2, 9):
         kz = k_idx.copy()
         kz[tok, dim] = 0
-        dk = np.zeros((t + 1, Di))
+        dk = np.zeros((len(k_idx), Di))
         ref.index_kl(d, t, q_idx, kz, q, k, sel, dk)
         kp, km = kz.copy(), kz.copy()
         kp[tok, dim] = bf([h])[0]
@@ -135,7 +137,7 @@ def test_tied_maximum_sends_the_gradient_to_the_first_token(ref):
     k_idx[2 * 128 + 9] = big
     t = nb * 128 - 1
     sel = np.array([[2, 5, 7] + [-1] * 13], np.int32)
-    dk = np.zeros((t + 1, Di))
+    dk = np.zeros((len(k_idx), Di))
     ref.index_kl(d, t, q_idx, k_idx, q, k, sel, dk)
     assert np.any(dk[2 * 128 + 9] != 0) and np.all(dk[2 * 128 + 70] == 0)
 
