@@ -336,7 +336,34 @@ def selection_quality(job, nrows, seed=7):
                           "ideal| / |ideal| per (query, group)"}
 
 
-def time_job(job, steps, warmup, world):
+def capture_step(job):
+    """One step of `job` captured into a CUDA graph (the C-ABI calls enqueue
+    kernels and memsets only, so they capture as they are), or None if the
+    capture fails."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    try:
+        with torch.cuda.stream(side):
+            job.step()                      # settles lazy per-function attributes
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            job.step()
+        torch.cuda.synchronize()
+        return g
+    except RuntimeError:
+        torch.cuda.synchronize()
+        return None
+
+
+def time_job(job, steps, warmup, world, graph=True):
+    """Warm-up, then two timed passes of `steps` steps each.  The eager pass
+    enqueues every call from Python with events around the index and attention
+    calls (their split, and the kernel count).  The headline pass replays the
+    same step captured into a CUDA graph, as a serving loop would, so that the
+    step is timed without per-call launch gaps; with graph=False (or if the
+    capture fails) the eager pass is the headline."""
     import torch
     for _ in range(warmup):
         job.step()
@@ -356,13 +383,32 @@ def time_job(job, steps, warmup, world):
     t1.record()
     torch.cuda.synchronize()
     barrier(world)
-    ck = clocks.stop()
     launches = job.msa.msa_kernel_launch_count() - n0
     job.msa.msa_workspace_status(job.ws)
-    total_ms = t0.elapsed_time(t1)
+    eager_ms = max_over_ranks(t0.elapsed_time(t1), world)
     idx_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
     att_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
-    return max_over_ranks(total_ms, world), idx_ms, att_ms, launches, ck
+    g = capture_step(job) if graph else None
+    total_ms, mode = eager_ms, "eager"
+    if g is not None:
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        job.msa.msa_workspace_status(job.ws)
+        barrier(world)
+        torch.cuda.synchronize()
+        t0.record()
+        for _ in range(steps):
+            g.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        job.msa.msa_workspace_status(job.ws)
+        total_ms, mode = max_over_ranks(t0.elapsed_time(t1), world), "cuda graph"
+        del g
+    ck = clocks.stop()
+    return {"total_ms": total_ms, "eager_ms": eager_ms, "idx_ms": idx_ms, "att_ms": att_ms,
+            "launches": launches, "clocks": ck, "mode": mode}
 
 
 class HostBuffers:
@@ -634,8 +680,9 @@ def measure(name, args, world, rank):
     import torch
     peaks, peak_kind = measured_peaks()
     job = Job(name, rank)
-    total_ms, idx_ms, att_ms, launches, clocks = time_job(job, args.steps, args.warmup, world)
-    ms = total_ms / args.steps
+    tj = time_job(job, args.steps, args.warmup, world, graph=not args.no_graph)
+    ms = tj["total_ms"] / args.steps
+    idx_ms, att_ms, launches, clocks = tj["idx_ms"], tj["att_ms"], tj["launches"], tj["clocks"]
     tokens = job.tokens() * world
     w = job.w
     pos = job.positions()
@@ -698,7 +745,8 @@ def measure(name, args, world, rank):
         e2e_ms, h2d, d2h = None, 0, 0
     cfg = {"workload": name, "batch": job.B, "ctx": job.L, "calls_per_step": len(job.calls),
            "queries_per_call": job.calls[0]["T"], "heads": H, "kv_heads": G, "head_dim": D,
-           "index_dim": DI, "block": BLK, "topk": 16, "l2": "inputs larger than L2 (no flush)"}
+           "index_dim": DI, "block": BLK, "topk": 16, "l2": "inputs larger than L2 (no flush)",
+           "launch": tj["mode"], "eager_ms_per_step": tj["eager_ms"] / args.steps}
     del job
     torch.cuda.empty_cache()
     cpu = None
@@ -765,6 +813,8 @@ def main():
     ap.add_argument("--quality-rows", type=int, default=64,
                     help="query positions sampled for the selection-quality figures (0: skip)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the eager step as the headline instead of its CUDA-graph replay")
     args = ap.parse_args()
     if args.secondary is None:
         args.secondary = ",".join(DEFAULT_SECONDARY) if args.workload == DEFAULT_WORKLOAD \

@@ -851,12 +851,22 @@ cudaError_t launch_dense_sel(const Shape& s, const Positions& pos, int chunk, in
 
 namespace {
 
-// Parts per (row, group) of the streaming attention: the fewest (of 1, 2, 4,
-// 8, 16) that give every CTA of the persistent grid a dozen work items or more.
+// Parts per (row, group) of the streaming attention: of 1, 2, 4, 8 and 16,
+// the one whose round-robin deal leaves the busiest CTA the least work,
+// counting a selected block as 8 and an item's own cost (its query copy, its
+// partials written and merged) as 1; ties go to fewer parts.
 int attn_stream_parts(int units, int ctas) {
-  int p = 1;
-  while (p < kTopk && (int64_t)units * p < 12 * (int64_t)ctas) p *= 2;
-  return p;
+  int best = 1;
+  int64_t best_load = INT64_MAX;
+  for (int p = 1; p <= kTopk; p *= 2) {
+    const int64_t items = (int64_t)units * p;
+    const int64_t load = (items + ctas - 1) / ctas * (8 * (kTopk / p) + 1);
+    if (load < best_load) {
+      best_load = load;
+      best = p;
+    }
+  }
+  return best;
 }
 
 template <int D, int NTH>
