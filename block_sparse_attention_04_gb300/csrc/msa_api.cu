@@ -172,23 +172,25 @@ int run_attn(const msa_params* p, const Shape& s, const Positions& pos, const ui
   return MSA_OK;
 }
 
-// Workspace of msa_dense_attn: status word, the chunk selection, the running
-// accumulators, then the attention scratch of the chosen kernel family.
+// Workspace of msa_dense_attn.  Tensor-core shapes: the status word only
+// (one query-outer kernel keeps everything else on chip).  Streaming shapes:
+// status word, the chunk selection, the running accumulators, then the
+// streaming attention's scratch.
 struct DensePlan {
   size_t sel_off, acc_o_off, acc_ml_off, scratch_off, total, part_rows;
 };
 
 DensePlan dense_plan_for(const msa_params* p) {
   DensePlan d{};
+  if (use_tc_attn(p)) {
+    d.total = kAlign;
+    return d;
+  }
   const Shape s = shape_of(p);
   const size_t rows = (size_t)p->B * p->T;
-  size_t att;
-  if (use_tc_attn(p)) {
-    att = align_up(tc_attn_workspace_bytes(s));
-  } else {
-    d.part_rows = attn_stream_part_rows(s, p->B * stream_pass_len(p));
-    att = align_up(d.part_rows * p->D * sizeof(float)) + align_up(d.part_rows * 2 * sizeof(float));
-  }
+  d.part_rows = attn_stream_part_rows(s, p->B * stream_pass_len(p));
+  const size_t att =
+      align_up(d.part_rows * p->D * sizeof(float)) + align_up(d.part_rows * 2 * sizeof(float));
   d.sel_off = kAlign;
   d.acc_o_off = d.sel_off + align_up(rows * p->G * MSA_TOPK * sizeof(int32_t));
   d.acc_ml_off = d.acc_o_off + align_up(rows * p->H * p->D * sizeof(float));
@@ -363,23 +365,21 @@ int msa_dense_attn(const msa_params* p, const uint16_t* q, const uint16_t* k_cac
   w.tc_bytes = d.total - d.scratch_off;
   if (cudaMemsetAsync(w.status, 0, sizeof(int), stream) != cudaSuccess) return MSA_ERR_CUDA;
   const Shape s = shape_of(p);
-  // chunks of 16 consecutive blocks, up to the last query's local block
+  if (use_tc_attn(p))
+    return cuda_status(launch_dense_tc(s, pos, q, k_cache, v_cache, out, w.status, stream));
+  // streaming shapes: chunks of 16 consecutive blocks, up to the last query's
+  // local block, each folded into fp32 running accumulators
   const int nchunks = (max_local_block(s, pos, 0, p->T) + MSA_TOPK) / MSA_TOPK;
   for (int c = 0; c < nchunks; ++c) {
     if (launch_dense_sel(s, pos, c, sel, stream) != cudaSuccess) return MSA_ERR_CUDA;
     DenseStep ds{reinterpret_cast<float*>(base + d.acc_o_off),
                  reinterpret_cast<float2*>(base + d.acc_ml_off), c == 0, c == nchunks - 1};
-    if (use_tc_attn(p)) {
-      if (launch_attn_tc(s, pos, q, k_cache, v_cache, sel, out, w, stream, &ds) != cudaSuccess)
+    const int tc = stream_pass_len(p);
+    for (int t0 = 0; t0 < p->T; t0 += tc) {
+      const int t1 = t0 + tc < p->T ? t0 + tc : p->T;
+      if (launch_attn_stream(s, pos, t0, t1, q, k_cache, v_cache, sel, out, w, stream, &ds) !=
+          cudaSuccess)
         return MSA_ERR_CUDA;
-    } else {
-      const int tc = stream_pass_len(p);
-      for (int t0 = 0; t0 < p->T; t0 += tc) {
-        const int t1 = t0 + tc < p->T ? t0 + tc : p->T;
-        if (launch_attn_stream(s, pos, t0, t1, q, k_cache, v_cache, sel, out, w, stream, &ds) !=
-            cudaSuccess)
-          return MSA_ERR_CUDA;
-      }
     }
   }
   return MSA_OK;

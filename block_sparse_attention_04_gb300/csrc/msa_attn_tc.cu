@@ -623,11 +623,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // ---- merge: one warp per (sequence, query, head) ----------------------------
-// DENSE: fold the pass's partials into the dense accumulators instead (one
-// chunk of msa_dense_attn).
-template <int D, bool DENSE>
-__global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnPass a, uint16_t* __restrict__ out,
-                                                            DenseStep ds) {
+template <int D>
+__global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnPass a, uint16_t* __restrict__ out) {
   constexpr int PER = D / 32;
   const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -676,14 +673,10 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnPass a, uint16_t
     }
   }
   uint16_t* dst = out + (((size_t)b * a.s.T + i) * H + h) * D + lane * PER;
-  if constexpr (DENSE) {
-    dense_fold<PER>(ds, ((size_t)b * a.s.T + i) * H + h, M, W, acc, lane, dst);
-  } else {
-    const float inv = 1.f / W;
+  const float inv = 1.f / W;
 #pragma unroll
-    for (int e = 0; e < PER; e += 2)
-      *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
-  }
+  for (int e = 0; e < PER; e += 2)
+    *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
 }
 
 struct AttnLayout {
@@ -714,8 +707,7 @@ AttnLayout attn_layout(const Shape& s) {
 template <int D>
 cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint16_t* q,
                                 const uint16_t* k, const uint16_t* v, const int32_t* sel,
-                                uint16_t* out, const Workspace& ws, cudaStream_t st,
-                                const DenseStep* dense) {
+                                uint16_t* out, const Workspace& ws, cudaStream_t st) {
   using C = AttnCfg<D>;
   const AttnLayout lay = attn_layout(s);
   char* base = ws.tc_base;
@@ -779,11 +771,7 @@ cudaError_t launch_attn_tc_impl(const Shape& s, const Positions& pos, const uint
     attn_tc_kernel<D><<<grid, kAttnThreads, C::kSmem, st>>>(tm_q, tm_k, tm_v, a);
     const int64_t warps = (int64_t)s.B * a.Tp * s.H;
     note_launches(1);
-    if (dense)
-      attn_tc_merge_kernel<D, true><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(a, out, *dense);
-    else
-      attn_tc_merge_kernel<D, false><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(a, out,
-                                                                                 DenseStep{});
+    attn_tc_merge_kernel<D><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(a, out);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -801,10 +789,9 @@ size_t tc_attn_workspace_bytes(const Shape& s) { return attn_layout(s).total; }
 
 cudaError_t launch_attn_tc(const Shape& s, const Positions& pos, const uint16_t* q,
                            const uint16_t* k, const uint16_t* v, const int32_t* sel,
-                           uint16_t* out, const Workspace& ws, cudaStream_t st,
-                           const DenseStep* dense) {
-  if (s.D == 128) return launch_attn_tc_impl<128>(s, pos, q, k, v, sel, out, ws, st, dense);
-  return launch_attn_tc_impl<64>(s, pos, q, k, v, sel, out, ws, st, dense);
+                           uint16_t* out, const Workspace& ws, cudaStream_t st) {
+  if (s.D == 128) return launch_attn_tc_impl<128>(s, pos, q, k, v, sel, out, ws, st);
+  return launch_attn_tc_impl<64>(s, pos, q, k, v, sel, out, ws, st);
 }
 
 }  // namespace msa

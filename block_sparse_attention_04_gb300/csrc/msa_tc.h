@@ -24,7 +24,12 @@ size_t tc_attn_workspace_bytes(const Shape& s);
 // attention, log-sum-exp merge), in passes of pass_len(s) queries.
 cudaError_t launch_attn_tc(const Shape& s, const Positions& pos, const uint16_t* q,
                            const uint16_t* k, const uint16_t* v, const int32_t* sel,
-                           uint16_t* out, const Workspace& ws, cudaStream_t st,
-                           const DenseStep* dense = nullptr);
+                           uint16_t* out, const Workspace& ws, cudaStream_t st);
+
+// Dense causal attention of every query of the call over all its causal
+// keys (query-outer tcgen05 kernel, O kept in tensor memory).
+cudaError_t launch_dense_tc(const Shape& s, const Positions& pos, const uint16_t* q,
+                            const uint16_t* k, const uint16_t* v, uint16_t* out, int* status,
+                            cudaStream_t st);
 
 }  // namespace msa

@@ -205,14 +205,16 @@ int msa_index_topk_noalloc(const msa_params *p, const uint16_t *q_idx, const uin
  * equation of "MiniMax 模型迭代与竞品分析" section 2, without selection).
  * M3 keeps its first three layers dense (section 3 of the same page:
  * sparse_attention_freq starts with three zeros), so a model built on this
- * library runs those layers here, on the caches its MSA layers use.  The
- * blocks are processed in chunks of 16 through the same attention kernels as
- * msa_sparse_attn (tensor-core KV-outer for prefill-sized calls, streaming
- * otherwise), each chunk's block partials folded into fp32 running
- * (output, max, sum) accumulators; out is bf16 (round to nearest even).
- * Arguments as for msa_sparse_attn without sel; ws of at least
- * msa_dense_workspace_bytes(p) bytes, 256-byte aligned (it holds
- * B*T*H*(D+2) fp32 accumulators besides the attention scratch). */
+ * library runs those layers here, on the caches its MSA layers use.
+ * Prefill-sized calls (the tensor-core choice of msa_sparse_attn) run one
+ * query-outer tensor-core kernel: 128 queries of a head pair at a time over
+ * every causal block, an online softmax with the output kept on chip.  Other
+ * calls process the blocks in chunks of 16 through the streaming attention,
+ * each chunk folded into fp32 running (output, max, sum) accumulators.  out
+ * is bf16 (round to nearest even).  Arguments as for msa_sparse_attn without
+ * sel; ws of at least msa_dense_workspace_bytes(p) bytes, 256-byte aligned
+ * (the status word; for the streaming calls also B*T*H*(D+2) fp32
+ * accumulators and the attention scratch). */
 size_t msa_dense_workspace_bytes(const msa_params *p);
 int msa_dense_attn(const msa_params *p, const uint16_t *q, const uint16_t *k_cache,
                    const uint16_t *v_cache, const int32_t *q_start, const int32_t *kv_len,

@@ -216,7 +216,11 @@ def test_dense_entry_point_validates_on_the_host(lib):
     n = msa.msa_dense_workspace_bytes(p)
     assert n > 0 and msa.msa_dense_workspace_bytes(P(D=96)) == 0
     p1 = P(T=64, max_blocks=4)
-    assert msa.msa_dense_workspace_bytes(p1) >= 64 * 48 * (128 + 2) * 4   # fp32 accumulators
+    # tensor-core shapes keep everything on chip: the status word only;
+    # streaming shapes add fp32 running accumulators
+    assert msa.msa_dense_workspace_bytes(p1) == 256
+    assert msa.msa_dense_workspace_bytes(P(T=64, max_blocks=4, kernels="streaming")) >= \
+        64 * 48 * (128 + 2) * 4
     a = 0x100000
     f = L.msa_dense_attn
     assert f(ctypes.byref(p), a, a, a, qs, kl, a, a, n, None) == OK
@@ -230,12 +234,12 @@ def test_dense_entry_point_validates_on_the_host(lib):
 
 
 def test_workspace_sizes_above_two_gigabytes_come_back_whole(lib):
-    # every *_workspace_bytes call returns size_t: a 32K dense call needs
-    # about 2.5 GB, more than a 32-bit return could hold
-    p = msa.params(1, 32768, 48, 8, 128, 64, 256)
+    # every *_workspace_bytes call returns size_t: a 64K dense call on the
+    # streaming kernels needs about 2.5 GB, more than a 32-bit return could hold
+    p = msa.params(1, 65536, 48, 8, 128, 64, 512, kernels="streaming")
     n = msa.msa_dense_workspace_bytes(p)
     assert n > (1 << 31)
-    assert n >= 32768 * 48 * 128 * 4                   # the fp32 output accumulators alone
+    assert n >= 65536 * 48 * 128 * 4                   # the fp32 output accumulators alone
     for f in (msa.msa_workspace_bytes, msa.msa_quality_workspace_bytes,
               msa.msa_index_kl_workspace_bytes, msa.msa_dense_workspace_bytes):
         assert f(p) > 0
