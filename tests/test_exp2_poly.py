@@ -59,12 +59,3 @@ def test_far_below_range_is_tiny_not_garbage():
     v = exp2_poly_host(x)
     assert np.all(np.isfinite(v)) and np.all(v >= 0) and np.all(v < 1e-37)
 
-
-def test_relative_error_up_to_two_to_the_eight():
-    # the dense kernel's lazily rescaled softmax evaluates 2^x for x up to 8
-    # (P up to 256 until the reference maximum is moved)
-    x = np.concatenate([np.linspace(0.0, 8.0, 800_001), np.arange(0, 9)]).astype(np.float32)
-    got = exp2_poly_host(x).astype(np.float64)
-    want = np.exp2(x.astype(np.float64))
-    rel = np.abs(got / want - 1)
-    assert rel.max() < 1e-4, rel.max()
