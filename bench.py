@@ -690,8 +690,8 @@ def measure(name, args, world, rank):
         fa = dense_flops(pos) * job.B
         sustained = ms * args.steps > 1000
         peak_tf = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "kernel": "dense attention (msa_dense_attn: 16-block chunks "
-                "through attn_tc_kernel + dense merge)",
+        roof = {"bound": "tensor", "kernel": "dense attention (msa_dense_attn: dense_tc_kernel, "
+                "query-outer with O in tensor memory)",
                 "achieved": fa / (att_ms / 1000.0) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
                 "traffic": None, "peak_kind": peak_kind + (" sustained" if sustained else " burst"),
                 "flops_per_step": fa}
