@@ -85,3 +85,29 @@ def test_pipeline_wait_expiry_is_reported_then_next_call_is_exact(msa, ref, kern
     assert _status(msa, ws) == 0
     assert_sel_equal(sel.cpu().numpy(), want_sel)
     assert_close(bf16_to_f64(out.cpu().numpy()), want_out)
+
+
+def test_dense_kernel_wait_expiry_is_reported_then_next_call_is_exact(msa, ref):
+    # the query-outer dense kernel (msa_dense_attn on a prefill-sized call)
+    import torch
+    wl = Workload(B=1, T=1000, H=12, G=4, D=128, Di=64, ctx=[3000], q_start=[2000])
+    want = ref.dense_attn(wl.dims(ref), wl.q, wl.k, wl.v, np.array(wl.q_start, np.int32),
+                          np.array(wl.kv_len, np.int32), wl.max_blocks)
+    dev = wl.device()
+    p = wl.params(msa, "tensorcore")
+    ws = msa.dense_workspace(p)
+    out = torch.zeros((wl.B, wl.T, wl.H, wl.D), dtype=torch.int16, device="cuda")
+    seen = []
+    try:
+        msa.msa_debug_set_wait_polls(1)
+        for _ in range(3):
+            msa.msa_dense_attn(p, dev["q"], dev["k"], dev["v"], wl.q_start, wl.kv_len, out, ws)
+            seen.append(_status(msa, ws))
+    finally:
+        msa.msa_debug_set_wait_polls(0)
+    torch.cuda.synchronize()
+    assert set(seen) <= {0, TIMEOUT} and TIMEOUT in seen, seen
+    out.fill_(0x7FC0)
+    msa.msa_dense_attn(p, dev["q"], dev["k"], dev["v"], wl.q_start, wl.kv_len, out, ws)
+    assert _status(msa, ws) == 0
+    assert_close(bf16_to_f64(out.cpu().numpy()), want)
