@@ -145,6 +145,29 @@ def test_decode_256k_all_sequences(ref):
     check_rows(ref, job, rows, kidx, attn_rows=rows[:8], kv=lazy_kv(job.seed, L // BLK))
 
 
+def test_dense_32k_sampled_rows(ref):
+    # msa_dense_attn over the whole 32K causal context (the query-outer
+    # tensor-core kernel), against the oracle's dense attention on >= 256 rows
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    job = run_job("dense_32k")
+    L, nb = job.L, job.L // BLK
+    kc = syn.kv_cache(job.seed, syn.TID_K, 0, nb, G, D)
+    vc = syn.kv_cache(job.seed, syn.TID_V, 0, nb, G, D)
+    ts = sample_positions(L, 256, 20261207)
+    d = ref.dims(H, G, D, DI)
+
+    def dense(t):
+        return ref.dense(d, t, syn.q_rows(job.seed, 0, t, t + 1, H, D)[0], kc, vc)
+
+    with ThreadPoolExecutor(os.cpu_count() or 4) as pool:
+        wants = list(pool.map(dense, ts))
+    err = np.concatenate([np.abs(bf16_to_f64(job.out[0, t].cpu().numpy()) - w).reshape(-1)
+                          for t, w in zip(ts, wants)])
+    record_err(err)
+    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (err.max(), err.mean())
+
+
 def test_prefill_1m_chunked_sampled(ref):
     job = run_job("prefill_1m")
     L = job.L
