@@ -39,7 +39,10 @@
  *     bytes, 256-byte aligned.  The library never allocates memory and keeps
  *     no state between calls except a status word inside ws.
  *   - Work is enqueued asynchronously on `stream`; nothing synchronises.
- *     Inputs must stay valid until the stream reaches the call's end.
+ *     Inputs must stay valid until the stream reaches the call's end.  The
+ *     calls enqueue only kernels and memsets, so a caller may capture them
+ *     into a CUDA graph and replay it (a graph holds the pointers, sizes and
+ *     positions of the captured call).
  *   - Every entry point returns MSA_OK or a negative msa_status.  Argument
  *     errors are found on the host before anything is enqueued.  A kernel
  *     whose bounded wait runs out records MSA_ERR_TIMEOUT in ws; read it with
