@@ -30,6 +30,8 @@ constexpr int kDQWarp = 0, kDKVWarp = 1, kDMmaWarp = 2, kDSoftWarp0 = 3;
 constexpr int kDenseThreads = 32 * 11;
 constexpr int kDKVStages = 2;
 constexpr float kLazyRescale = 8.f;  // log2 of the growth of P tolerated before O is rescaled
+constexpr int kDItemRing = 4;        // item ids published by the Q warp, ahead of use
+constexpr int kDItemReaders = 10;    // the K/V lane, the MMA warp, the 8 softmax warps
 
 struct DenseArgs {
   Shape s;
@@ -37,6 +39,7 @@ struct DenseArgs {
   int nqt;      // 128-query tiles per sequence
   int npair;    // head pairs per KV group: ceil(H/G / 2)
   int nitems;   // nqt * B * G * npair
+  int* next_item;  // shared counter of taken items (zeroed with the status word)
   uint16_t* out;
   int* status;
   uint32_t wait_polls;  // poll cap of the pipeline waits (0: wall-clock bound only)
@@ -47,11 +50,12 @@ struct DenseCfg {
   static constexpr int kNHalf = D / 64;
   static constexpr int kHalf = 128 * 128;       // one box: 128 rows x 64 dims (16 KiB)
   static constexpr int kTile = kNHalf * kHalf;  // 128 rows x D: a Q tile, a K or a V block
-  static constexpr int kSmem = 2 * kTile + 2 * kDKVStages * kTile + 256 + 1024;
+  static constexpr int kSmem = 2 * kTile + 2 * kDKVStages * kTile + 512 + 1024;
   static constexpr uint32_t kTmemCols = 512;
 };
 
 // Item it, heaviest first: query tiles from the last (most key blocks) down.
+// CTAs take items from a shared counter as they go (greedy list scheduling).
 struct DenseItem {
   int b, g, ha, hb, qt, nblk;
   bool hb_real;  // false: the group has an odd head count and chain 1 repeats ha
@@ -96,7 +100,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
   uint64_t* p_full = s_full + 2;                // per chain: P written over S (O rescaled)
   uint64_t* o_full = p_full + 2;                // per chain: the item's last P.V is done
   uint64_t* bar_fin = o_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_fin + 1);
+  uint64_t* it_full = bar_fin + 1;              // kDItemRing: an item id is published
+  uint64_t* it_empty = it_full + kDItemRing;    // kDItemRing: every reader has it
+  int* item_ring = reinterpret_cast<int*>(it_empty + kDItemRing);  // ids, -1: no more
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(item_ring + kDItemRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -115,6 +122,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       mbar_init(&o_full[c], 1);
     }
     mbar_init(bar_fin, 1);
+    for (int i = 0; i < kDItemRing; ++i) {
+      mbar_init(&it_full[i], 1);
+      mbar_init(&it_empty[i], kDItemReaders);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -131,10 +142,27 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
   if (warp == kDQWarp) {
     // ------------------------------------------------------- Q TMA (warp 0)
     if (lane == 0) {
+      // Takes the items: publishes item k + 1's id (-1 once none is left, or
+      // after an abort) before it loads item k's Q, so that the K/V copies
+      // of the next item can start during this one.
       const uint64_t pol = l2_policy_evict_first();
+      int cur = atomicAdd(a.next_item, 1);
+      if (cur >= a.nitems) cur = -1;
+      item_ring[0] = cur;
+      mbar_arrive(&it_full[0]);
       int k = 0;
-      for (int it = blockIdx.x; it < a.nitems && !*abort_flag; it += gridDim.x, ++k) {
-        const DenseItem d = dense_item(a, it);
+      for (; cur >= 0; ++k) {
+        const int r = k + 1, slot = r % kDItemRing;
+        if (r >= kDItemRing &&
+            !mbar_wait(&it_empty[slot], ((r / kDItemRing) - 1) & 1, a.status, a.wait_polls)) {
+          *abort_flag = 1;
+          break;
+        }
+        int nx = *abort_flag ? a.nitems : atomicAdd(a.next_item, 1);
+        if (nx >= a.nitems) nx = -1;
+        item_ring[slot] = nx;
+        mbar_arrive(&it_full[slot]);
+        const DenseItem d = dense_item(a, cur);
         if (k > 0 && !mbar_wait(q_empty, (k - 1) & 1, a.status, a.wait_polls)) {
           *abort_flag = 1;
           break;
@@ -147,6 +175,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
           tma_load_3d_hint(smem_u32(sQ + C::kTile + h * C::kHalf), &tm_q, q_full, h * 64, d.hb, z,
                            pol);
         }
+        cur = nx;
       }
       // no copy may still be landing when the CTA exits
       if (k > 0) mbar_wait(q_full, (k - 1) & 1, nullptr);
@@ -156,7 +185,15 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     if (lane == 0) {
       int n = 0;
       bool ok = true, k_only = false;  // k_only: step n's K is loaded, its V is not
-      for (int it = blockIdx.x; it < a.nitems && ok && !*abort_flag; it += gridDim.x) {
+      for (int ki = 0; ok && !*abort_flag; ++ki) {
+        const int slot = ki % kDItemRing;
+        if (!mbar_wait(&it_full[slot], (ki / kDItemRing) & 1, a.status, a.wait_polls)) {
+          ok = false;
+          break;
+        }
+        const int it = item_ring[slot];
+        mbar_arrive(&it_empty[slot]);
+        if (it < 0) break;
         const DenseItem d = dense_item(a, it);
         for (int kb = 0; kb < d.nblk; ++kb, ++n) {
           const int ks = n % kDKVStages;
@@ -204,8 +241,16 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     const uint64_t vdesc0 = smem_desc(smem_u32(sV), C::kHalf, 1024, kSwizzle128B);
     int n = 0, k = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < a.nitems && ok; it += gridDim.x, ++k) {
+    for (; ok; ++k) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+      const int slot = k % kDItemRing;
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&it_full[slot], (k / kDItemRing) & 1, a.status, a.wait_polls));
+      if (!ok) break;
+      const int it = item_ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&it_empty[slot]);
+      if (it < 0) break;
       const DenseItem d = dense_item(a, it);
       ok = __all_sync(0xffffffffu, mbar_wait(q_full, k & 1, a.status, a.wait_polls));
       if (!ok) break;
@@ -280,7 +325,17 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     const float sl = a.s.scale * kLog2e;
     int n = 0, k = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < a.nitems && ok; it += gridDim.x, ++k) {
+    for (; ok; ++k) {
+      const int slot = k % kDItemRing;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&it_full[slot], (k / kDItemRing) & 1, a.status, a.wait_polls))) {
+        ok = false;
+        break;
+      }
+      const int it = item_ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&it_empty[slot]);
+      if (it < 0) break;
       const DenseItem d = dense_item(a, it);
       const int i = d.qt * 128 + r;
       const bool valid = i < T && (c == 0 || d.hb_real);
@@ -438,6 +493,8 @@ cudaError_t launch_dense_tc_impl(const Shape& s, const Positions& pos, const uin
                                  const uint16_t* k, const uint16_t* v, uint16_t* out, int* status,
                                  cudaStream_t st) {
   using C = DenseCfg<D>;
+  // the item counter sits in the word after the status word; both are zeroed
+  if (cudaMemsetAsync(status, 0, 2 * sizeof(int), st) != cudaSuccess) return cudaErrorUnknown;
   CUtensorMap tm_q, tm_k, tm_v;
   {
     // q as (D dims, H heads, B*T queries): one box = 128 queries x 64 dims
@@ -462,6 +519,7 @@ cudaError_t launch_dense_tc_impl(const Shape& s, const Positions& pos, const uin
   a.nqt = (s.T + 127) / 128;
   a.npair = (s.H / s.G + 1) / 2;
   a.nitems = a.nqt * s.B * s.G * a.npair;
+  a.next_item = status + 1;
   a.out = out;
   a.status = status;
   a.wait_polls = debug_wait_polls();
