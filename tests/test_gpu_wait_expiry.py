@@ -59,11 +59,16 @@ def test_pipeline_wait_expiry_is_reported_then_next_call_is_exact(msa, ref, kern
     ref_sel = torch.from_numpy(want_sel).cuda()
 
     seen = {"index": [], "attn": []}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")   # larger than L2
     try:
         msa.msa_debug_set_wait_polls(1)
-        for _ in range(3):
+        for i in range(4):
+            # every call starts with cold caches, so that its copies take long
+            # enough for a one-poll wait to run out
+            flush.fill_(i)
             msa.msa_index_topk(p, dev["q_idx"], dev["k_idx"], wl.q_start, wl.kv_len, sel, ws)
             seen["index"].append(_status(msa, ws))
+            flush.fill_(i + 1)
             msa.msa_sparse_attn(p, dev["q"], dev["k"], dev["v"], ref_sel, wl.q_start, wl.kv_len,
                                 out, ws)
             seen["attn"].append(_status(msa, ws))
@@ -98,9 +103,11 @@ def test_dense_kernel_wait_expiry_is_reported_then_next_call_is_exact(msa, ref):
     ws = msa.dense_workspace(p)
     out = torch.zeros((wl.B, wl.T, wl.H, wl.D), dtype=torch.int16, device="cuda")
     seen = []
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")   # larger than L2
     try:
         msa.msa_debug_set_wait_polls(1)
-        for _ in range(3):
+        for i in range(4):
+            flush.fill_(i)
             msa.msa_dense_attn(p, dev["q"], dev["k"], dev["v"], wl.q_start, wl.kv_len, out, ws)
             seen.append(_status(msa, ws))
     finally:
