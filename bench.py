@@ -458,7 +458,7 @@ class HostBuffers:
         self.regs = []
 
 
-def time_e2e(job, steps, world, host_alloc="thp"):
+def time_e2e(job, steps, world, host_alloc="thp", graph=True):
     """Same step through the C ABI with host buffers: pinned H2D of the step's
     inputs and D2H of its outputs inside the timed region."""
     import torch
@@ -522,15 +522,37 @@ def time_e2e(job, steps, world, host_alloc="thp"):
 
     run(1)                              # untimed warm-up of the copy path
     torch.cuda.synchronize()
+    # A single call per step (decode, one-call prefill) is replayed as a CUDA
+    # graph of its copies and calls, as a serving loop would run it; each
+    # replay moves the same bytes.  The pipelined chunked prefill stays eager.
+    g, mode = None, "eager"
+    if graph and not pipelined:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                run(1)
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()
+            mode = "cuda graph"
+        except RuntimeError:
+            torch.cuda.synchronize()
+            g = None
     barrier(world)
     t0.record()
-    run(steps)
+    if g is not None:
+        for _ in range(steps):
+            g.replay()
+    else:
+        run(steps)
     t1.record()
     torch.cuda.synchronize()
     ms = max_over_ranks(t0.elapsed_time(t1), world) / steps
-    del host, sel_h, out_h
+    del g, host, sel_h, out_h
     bufs.release()
-    return ms, h2d, d2h
+    return ms, h2d, d2h, mode
 
 
 # ---------------------------------------------------------------- CPU arm --
@@ -740,9 +762,10 @@ def measure(name, args, world, rank):
     quality = selection_quality(job, args.quality_rows) \
         if args.quality_rows > 0 and job.mode == "sparse" else None
     if job.mode == "sparse":
-        e2e_ms, h2d, d2h = time_e2e(job, max(1, min(args.steps, 3)), world, args.host_alloc)
+        e2e_ms, h2d, d2h, e2e_mode = time_e2e(job, max(1, min(args.steps, 3)), world,
+                                              args.host_alloc, graph=not args.no_graph)
     else:
-        e2e_ms, h2d, d2h = None, 0, 0
+        e2e_ms, h2d, d2h, e2e_mode = None, 0, 0, None
     cfg = {"workload": name, "batch": job.B, "ctx": job.L, "calls_per_step": len(job.calls),
            "queries_per_call": job.calls[0]["T"], "heads": H, "kv_heads": G, "head_dim": D,
            "index_dim": DI, "block": BLK, "topk": 16, "l2": "inputs larger than L2 (no flush)",
@@ -761,7 +784,8 @@ def measure(name, args, world, rank):
                 "value": tokens / (e2e_ms / 1000.0), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "host_buffers": {"thp": "page-locked transparent huge pages",
-                                 "torch": "torch pinned allocator"}[args.host_alloc]},
+                                 "torch": "torch pinned allocator"}[args.host_alloc],
+                "launch": e2e_mode},
             "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
             "selection_quality": quality}
 
