@@ -247,8 +247,9 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       ok = __all_sync(0xffffffffu,
                       mbar_wait(&it_full[slot], (k / kDItemRing) & 1, a.status, a.wait_polls));
       if (!ok) break;
-      const int it = item_ring[slot];
-      __syncwarp();
+      // every lane's read of the slot is consumed (by the shuffle) before the
+      // slot is handed back, so no read can still be pending when it is rewritten
+      const int it = __shfl_sync(0xffffffffu, item_ring[slot], 0);
       if (lane == 0) mbar_arrive(&it_empty[slot]);
       if (it < 0) break;
       const DenseItem d = dense_item(a, it);
@@ -332,8 +333,9 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         ok = false;
         break;
       }
-      const int it = item_ring[slot];
-      __syncwarp();
+      // every lane's read of the slot is consumed (by the shuffle) before the
+      // slot is handed back, so no read can still be pending when it is rewritten
+      const int it = __shfl_sync(0xffffffffu, item_ring[slot], 0);
       if (lane == 0) mbar_arrive(&it_empty[slot]);
       if (it < 0) break;
       const DenseItem d = dense_item(a, it);

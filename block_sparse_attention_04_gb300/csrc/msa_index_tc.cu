@@ -318,8 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) *abort_flag = 1;
           break;
         }
-        const int it = item_ring[slot];
-        __syncwarp();
+        // every lane's read of the slot is consumed (by the shuffle) before the
+        // slot is handed back, so no read can still be pending when it is rewritten
+        const int it = __shfl_sync(0xffffffffu, item_ring[slot], 0);
         if (lane == 0) mbar_arrive(&it_empty[slot]);
         if (it < 0) break;
         int b, p, sp, k0, k1;
@@ -390,8 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int slot = ki % kItemRing;
       const bool okw =
           __all_sync(0xffffffffu, mbar_wait(&it_full[slot], (ki / kItemRing) & 1, a.status, a.wait_polls));
-      const int it = item_ring[slot];
-      __syncwarp();
+      // every lane's read of the slot is consumed (by the shuffle) before the
+      // slot is handed back, so no read can still be pending when it is rewritten
+      const int it = __shfl_sync(0xffffffffu, item_ring[slot], 0);
       if (lane == 0) mbar_arrive(&it_empty[slot]);
       if (!named_bar_and(1, 512, okw)) {
         stop = true;
