@@ -110,6 +110,14 @@ def test_quality_long_context(msa, ref):
     assert np.all(got[0] < 0.9) and np.all(got[1] >= 0)
 
 
+def test_quality_full_128k_context(msa, ref):
+    # the last 16 queries of a 131072-token context (1024 blocks, the 128K
+    # prefill's longest rows): every block's mass over the whole context
+    wl = Workload(B=1, T=16, H=48, G=8, D=128, Di=64, ctx=[131072], q_start=[131056])
+    sel = oracle_selection(ref, wl)
+    check_quality(ref, wl, sel, run_quality(msa, wl, sel))
+
+
 def test_quality_decode_batch_ragged_contexts(msa, ref):
     ctx = [1, 127, 128, 129, 2048, 2049, 5000, 9000]
     wl = Workload(B=len(ctx), T=1, H=48, G=8, D=128, Di=64, ctx=ctx,
