@@ -58,6 +58,14 @@ def test_kl_prefill_m2_layout(msa, ref):
     check(ref, wl, sel, run_kl(msa, wl, sel))
 
 
+def test_kl_full_128k_context(msa, ref):
+    # 64 queries at the end of a 131072-token context (1024 blocks), the 128K
+    # prefill's longest rows; the gradient dK_idx spans the whole context
+    wl = Workload(B=1, T=64, H=48, G=8, D=128, Di=64, ctx=[131072], q_start=[131008])
+    sel, _ = wl.oracle(ref)
+    check(ref, wl, sel, run_kl(msa, wl, sel))
+
+
 def test_kl_long_context_chunk_and_decode_batch(msa, ref):
     wl = Workload(B=1, T=200, H=12, G=4, D=128, Di=64, ctx=[9000], q_start=[8800])
     sel, _ = wl.oracle(ref)
