@@ -56,6 +56,8 @@ WORKLOADS = {
     "decode_256k_paged": dict(cfg=3, kind="decode", B=64, L=262144, mode="paged"),
 }
 DEFAULT_WORKLOAD = "prefill_1m"
+# queries per attention call when the e2e leg splits a single long prefill
+E2E_SLICE = 8192
 # measured in the same run and nested in the default line, under these keys
 DEFAULT_SECONDARY = ("prefill_128k", "decode_256k")
 NESTED_KEY = {"prefill_128k": "prefill_128k", "decode_256k": "decode"}
@@ -476,12 +478,69 @@ def time_e2e(job, steps, world, host_alloc="thp", graph=True):
     d2h = sel_h.numel() * 4 + out_h.numel() * 2
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    pipelined = job.w["kind"] != "decode" and len(job.calls) > 1 and job.B == 1
-    if pipelined:
+    prefill = job.w["kind"] != "decode" and job.B == 1 and job.mode == "sparse"
+    pipelined = prefill and len(job.calls) > 1
+    # A single long prefill call: one index call over all its queries, then
+    # the attention as consecutive calls of E2E_SLICE queries each (the same
+    # kernels and results as one call, which runs in passes of that length),
+    # so that the query rows go up and the outputs come back while other
+    # slices compute.
+    sliced = prefill and len(job.calls) == 1 and job.calls[0]["T"] > E2E_SLICE
+    if pipelined or sliced:
         comp = torch.cuda.current_stream()
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    if sliced:
+        c0 = job.calls[0]
+        slice_params = job.msa.params(1, E2E_SLICE, H, G, D, DI, job.nb)
+        tail = c0["T"] % E2E_SLICE
+        tail_params = job.msa.params(1, tail, H, G, D, DI, job.nb) if tail else None
+
+    def record(stream):
+        e = torch.cuda.Event()
+        e.record(stream)
+        return e
+
+    def run_sliced(n):
+        c = c0
+        st, T = c["q_start"][0], c["T"]
+        msa = job.msa
+        for _ in range(n):
+            s_in.wait_stream(comp)      # steps do not overlap
+            with torch.cuda.stream(s_in):
+                job.dev["q_idx"].copy_(host["q_idx"], non_blocking=True)
+                job.dev["k_idx"].copy_(host["k_idx"], non_blocking=True)
+                ev_idx = record(s_in)
+                job.dev["k"].copy_(host["k"], non_blocking=True)
+                job.dev["v"].copy_(host["v"], non_blocking=True)
+                ev_q = []
+                for a in range(0, T, E2E_SLICE):
+                    job.dev["q"][:, a:a + E2E_SLICE].copy_(host["q"][:, a:a + E2E_SLICE],
+                                                           non_blocking=True)
+                    ev_q.append(record(s_in))
+            comp.wait_event(ev_idx)
+            msa.msa_index_topk(job.params, job.dev["q_idx"], job.dev["k_idx"], c["q_start"],
+                               c["kv_len"], job.sel, job.ws)
+            ev_sel = record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_sel)
+                sel_h.copy_(job.sel, non_blocking=True)
+            for j, a in enumerate(range(0, T, E2E_SLICE)):
+                n_j = min(E2E_SLICE, T - a)
+                comp.wait_event(ev_q[j])    # after K/V, on the same stream
+                msa.msa_sparse_attn(slice_params if n_j == E2E_SLICE else tail_params,
+                                    job.dev["q"][:, a:a + n_j], job.dev["k"], job.dev["v"],
+                                    job.sel[:, a:a + n_j], [st + a], c["kv_len"],
+                                    job.out[:, a:a + n_j], job.ws)
+                ev_o = record(comp)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_o)
+                    out_h[:, a:a + n_j].copy_(job.out[:, a:a + n_j], non_blocking=True)
+            comp.wait_stream(s_out)
 
     def run(n):
+        if sliced:
+            run_sliced(n)
+            return
         if not pipelined:
             for _ in range(n):
                 for nm in names:
@@ -522,11 +581,12 @@ def time_e2e(job, steps, world, host_alloc="thp", graph=True):
 
     run(1)                              # untimed warm-up of the copy path
     torch.cuda.synchronize()
-    # A single call per step (decode, one-call prefill) is replayed as a CUDA
-    # graph of its copies and calls, as a serving loop would run it; each
-    # replay moves the same bytes.  The pipelined chunked prefill stays eager.
+    # A single call per step (decode, a prefill of one slice) is replayed as a
+    # CUDA graph of its copies and calls, as a serving loop would run it; each
+    # replay moves the same bytes.  The pipelined and sliced prefills, whose
+    # copies overlap the compute on three streams, stay eager.
     g, mode = None, "eager"
-    if graph and not pipelined:
+    if graph and not pipelined and not sliced:
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         try:
@@ -552,6 +612,10 @@ def time_e2e(job, steps, world, host_alloc="thp", graph=True):
     ms = max_over_ranks(t0.elapsed_time(t1), world) / steps
     del g, host, sel_h, out_h
     bufs.release()
+    if pipelined:
+        mode += ", copies pipelined per chunk"
+    elif sliced:
+        mode += ", index call then attention in %d-query calls, copies pipelined" % E2E_SLICE
     return ms, h2d, d2h, mode
 
 

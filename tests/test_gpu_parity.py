@@ -126,6 +126,34 @@ def test_chunked_prefill_matches_whole(msa, ref, kernels):
         assert_close(out[0], want_out[0, c0:c1])
 
 
+def test_attention_in_slices_equals_one_call(msa):
+    # msa_sparse_attn over a long prefill in consecutive calls of fewer queries
+    # (aligned with the tensor-core path's 8192-query passes, or not) gives
+    # the same bits as one call: every query-head row's scores, softmax and
+    # partial outputs depend on its own row and selection only.  The bench's
+    # end-to-end leg splits a single long prefill this way.
+    import torch
+    import msa_synth.device as sd
+    L, H_, G_, D_, DI_ = 19968, 48, 8, 128, 64
+    nb = L // 128
+    dev = sd.make_inputs(1, H_, G_, D_, DI_, nb, L, syn.BASE_SEED + 11)
+    p = msa.params(1, L, H_, G_, D_, DI_, nb)
+    ws = msa.workspace(p)
+    sel = torch.empty((1, L, G_, 16), dtype=torch.int32, device="cuda")
+    out = torch.empty((1, L, H_, D_), dtype=torch.int16, device="cuda")
+    msa.msa_index_topk(p, dev["q_idx"], dev["k_idx"], [0], [L], sel, ws)
+    msa.msa_sparse_attn(p, dev["q"], dev["k"], dev["v"], sel, [0], [L], out, ws)
+    for step in (8192, 5000):
+        got = torch.full_like(out, -1)
+        for a in range(0, L, step):
+            n = min(step, L - a)
+            ps = msa.params(1, n, H_, G_, D_, DI_, nb)
+            msa.msa_sparse_attn(ps, dev["q"][:, a:a + n], dev["k"], dev["v"], sel[:, a:a + n],
+                                [a], [L], got[:, a:a + n], ws)
+        torch.cuda.synchronize()
+        assert torch.equal(got, out), step
+
+
 @pytest.mark.parametrize("kernels", KERNELS)
 def test_decode_batch_ragged_contexts(msa, ref, kernels):
     ctx = [1, 127, 128, 129, 2048, 2049, 5000, 9000]
