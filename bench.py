@@ -489,6 +489,8 @@ def time_e2e(job, steps, world, host_alloc="thp", graph=True):
     if pipelined or sliced:
         comp = torch.cuda.current_stream()
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    else:
+        side_in, side_out = torch.cuda.Stream(), torch.cuda.Stream()
     if sliced:
         c0 = job.calls[0]
         slice_params = job.msa.params(1, E2E_SLICE, H, G, D, DI, job.nb)
@@ -542,12 +544,31 @@ def time_e2e(job, steps, world, host_alloc="thp", graph=True):
             run_sliced(n)
             return
         if not pipelined:
+            # one call: the index inputs go up first; the attention's inputs
+            # follow on a side stream while the index call runs, and sel comes
+            # back on another while the attention runs
+            cur = torch.cuda.current_stream()
+            first = [nm for nm in ("q_idx", "k_idx") if nm in names]
+            rest = [nm for nm in names if nm not in first]
+            (c,) = job.calls
+            q_idx, k_idx, q, k, v, sel, out = job.views(c)
             for _ in range(n):
-                for nm in names:
+                for nm in first:
                     job.dev[nm].copy_(host[nm], non_blocking=True)
-                job.step()
-                sel_h.copy_(job.sel, non_blocking=True)
+                side_in.wait_stream(cur)
+                with torch.cuda.stream(side_in):
+                    for nm in rest:
+                        job.dev[nm].copy_(host[nm], non_blocking=True)
+                job.msa.msa_index_topk(job.params, q_idx, k_idx, c["q_start"], c["kv_len"], sel,
+                                       job.ws)
+                side_out.wait_stream(cur)
+                with torch.cuda.stream(side_out):
+                    sel_h.copy_(job.sel, non_blocking=True)
+                cur.wait_stream(side_in)
+                job.msa.msa_sparse_attn(job.params, q, k, v, sel, c["q_start"], c["kv_len"], out,
+                                        job.ws)
                 out_h.copy_(job.out, non_blocking=True)
+                cur.wait_stream(side_out)
             return
         # chunked prefill, pipelined as a caller of the C ABI would run it:
         # chunk c's inputs (its q_idx and q rows, the k_idx rows and K/V blocks
@@ -616,6 +637,8 @@ def time_e2e(job, steps, world, host_alloc="thp", graph=True):
         mode += ", copies pipelined per chunk"
     elif sliced:
         mode += ", index call then attention in %d-query calls, copies pipelined" % E2E_SLICE
+    else:
+        mode += ", attention inputs up and sel down beside the calls"
     return ms, h2d, d2h, mode
 
 
