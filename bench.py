@@ -926,9 +926,9 @@ def main():
                     help="comma-separated workloads reported in the same line (default: "
                          "prefill_128k,decode_256k when the workload is the default one; "
                          "'none' to skip)")
-    ap.add_argument("--host-alloc", choices=["thp", "torch"], default="torch",
-                    help="host buffers of the e2e leg: torch's pinned allocator (default) or "
-                         "page-locked transparent huge pages (measured slower on GB300)")
+    ap.add_argument("--host-alloc", choices=["thp", "torch"], default="thp",
+                    help="host buffers of the e2e leg: page-locked transparent huge pages "
+                         "(default) or torch's pinned allocator")
     ap.add_argument("--quality-rows", type=int, default=64,
                     help="query positions sampled for the selection-quality figures (0: skip)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
