@@ -421,10 +421,19 @@ class HostBuffers:
     kind "thp": anonymous memory advised onto transparent huge pages (the
     host's PMD size), aligned to that size, then page-locked with
     cudaHostRegister, so that a copy walks few, large physical runs; kind
-    "torch": torch's pinned allocator (cudaHostAlloc)."""
+    "torch": torch's pinned allocator (cudaHostAlloc); kind "auto": a "thp"
+    buffer, kept if a copy of all of it runs at AUTO_MIN_GBS or more (or it
+    is small), else the faster of it and a "torch" buffer (after a long run
+    of other work the host's free memory can be so scattered that either
+    kind copies slowly)."""
+
+    AUTO_MIN_GBS = 150.0
+    AUTO_MIN_BYTES = 256 << 20          # smaller copies are latency-bound: not probed
 
     def __init__(self, kind):
         self.kind, self.maps, self.regs = kind, [], []
+        self.used = []                  # the kind each buffer ended up with
+        self.probed = {"h2d": [], "d2h": []}  # GB/s of the buffers kept
         self.huge = 2 << 20
         try:
             with open("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size") as f:
@@ -432,11 +441,31 @@ class HostBuffers:
         except (OSError, ValueError):
             pass
 
-    def empty(self, shape, dtype):
-        import mmap
+    def empty(self, shape, dtype, to_device=True):
+        """to_device: the buffer is a copy source (H2D) rather than a target."""
         import torch
         if self.kind == "torch":
+            self.used.append("torch")
             return torch.empty(shape, dtype=dtype, pin_memory=True)
+        t = self._thp(shape, dtype)
+        kind = "thp"
+        if self.kind == "auto" and t.numel() * t.element_size() >= self.AUTO_MIN_BYTES:
+            bw = self._probe(t, to_device)
+            if bw < self.AUTO_MIN_GBS:
+                t2 = torch.empty(shape, dtype=dtype, pin_memory=True)
+                bw2 = self._probe(t2, to_device)
+                if bw2 > bw:
+                    self._unregister(t.data_ptr())
+                    del t
+                    self.maps.pop()         # the mapping goes once nothing views it
+                    t, kind, bw = t2, "torch", bw2
+            self.probed["h2d" if to_device else "d2h"].append(bw)
+        self.used.append(kind)
+        return t
+
+    def _thp(self, shape, dtype):
+        import mmap
+        import torch
         item = torch.empty((), dtype=dtype).element_size()
         n = int(np.prod(shape)) * item
         span = (n + 2 * self.huge - 1) // self.huge * self.huge
@@ -455,6 +484,38 @@ class HostBuffers:
         self.regs.append(t.data_ptr())
         return t
 
+    @staticmethod
+    def _probe(t, to_device, chunk=1 << 30):
+        """Copy bandwidth (GB/s) of the whole of t (page placement differs
+        along a buffer), in copies of up to `chunk` bytes."""
+        import torch
+        flat = t.view(-1).view(torch.uint8)
+        n = min(flat.numel(), chunk)
+        d = torch.empty(n, dtype=torch.uint8, device="cuda")
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for a in range(0, flat.numel(), chunk):
+            h = flat[a:a + chunk]
+            if to_device:
+                d[:h.numel()].copy_(h, non_blocking=True)
+            else:
+                h.copy_(d[:h.numel()], non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        del d
+        return flat.numel() / (e0.elapsed_time(e1) / 1e3) / 1e9
+
+    def _unregister(self, ptr):
+        import torch
+        torch.cuda.cudart().cudaHostUnregister(ptr)
+        self.regs.remove(ptr)
+
+    def describe(self):
+        kinds = {"thp": "page-locked transparent huge pages", "torch": "torch pinned allocator"}
+        used = sorted(set(self.used))
+        return " + ".join(kinds[k] for k in used) if used else kinds.get(self.kind, self.kind)
+
     def release(self):
         import torch
         for ptr in self.regs:
@@ -462,7 +523,7 @@ class HostBuffers:
         self.regs = []
 
 
-def time_e2e(job, steps, world, host_alloc="thp", graph=True):
+def time_e2e(job, steps, world, host_alloc="auto", graph=True):
     """Same step through the C ABI with host buffers: pinned H2D of the step's
     inputs and D2H of its outputs inside the timed region."""
     import torch
@@ -474,8 +535,8 @@ def time_e2e(job, steps, world, host_alloc="thp", graph=True):
     host = {n: bufs.empty(job.dev[n].shape, torch.int16) for n in names}
     for n in names:
         host[n].copy_(job.dev[n])
-    sel_h = bufs.empty(job.sel.shape, torch.int32)
-    out_h = bufs.empty(job.out.shape, torch.int16)
+    sel_h = bufs.empty(job.sel.shape, torch.int32, to_device=False)
+    out_h = bufs.empty(job.out.shape, torch.int16, to_device=False)
     h2d = sum(host[n].numel() * 2 for n in names)
     d2h = sel_h.numel() * 4 + out_h.numel() * 2
     t0 = torch.cuda.Event(enable_timing=True)
@@ -489,7 +550,6 @@ def time_e2e(job, steps, world, host_alloc="thp", graph=True):
     # slices compute.
     sliced = prefill and len(job.calls) == 1 and job.calls[0]["T"] > E2E_SLICE
     if pipelined or sliced:
-        comp = torch.cuda.current_stream()
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     else:
         side_in, side_out = torch.cuda.Stream(), torch.cuda.Stream()
@@ -508,6 +568,7 @@ def time_e2e(job, steps, world, host_alloc="thp", graph=True):
         c = c0
         st, T = c["q_start"][0], c["T"]
         msa = job.msa
+        comp = torch.cuda.current_stream()
         for _ in range(n):
             s_in.wait_stream(comp)      # steps do not overlap
             with torch.cuda.stream(s_in):
@@ -578,6 +639,7 @@ def time_e2e(job, steps, world, host_alloc="thp", graph=True):
         # compute stream once they have landed, and its out and sel rows come
         # back on a third stream while the next chunk computes.  The same
         # bytes move as in the serial form; only their overlap differs.
+        comp = torch.cuda.current_stream()
         for _ in range(n):
             s_in.wait_stream(comp)      # steps do not overlap
             for c in job.calls:
@@ -606,8 +668,9 @@ def time_e2e(job, steps, world, host_alloc="thp", graph=True):
     torch.cuda.synchronize()
     # A single call per step (decode, a prefill of one slice) is replayed as a
     # CUDA graph of its copies and calls, as a serving loop would run it; each
-    # replay moves the same bytes.  The pipelined and sliced prefills, whose
-    # copies overlap the compute on three streams, stay eager.
+    # replay moves the same bytes.  The pipelined and sliced prefills stay
+    # eager: replayed as graphs, their copies ran at a third of the speed of
+    # the same eager copies in runs that followed the GPU test suite.
     g, mode = None, "eager"
     if graph and not pipelined and not sliced:
         side = torch.cuda.Stream()
@@ -634,6 +697,11 @@ def time_e2e(job, steps, world, host_alloc="thp", graph=True):
     torch.cuda.synchronize()
     ms = max_over_ranks(t0.elapsed_time(t1), world) / steps
     del g, host, sel_h, out_h
+    described = bufs.describe()
+    probed = {k: round(min(v), 1) for k, v in bufs.probed.items() if v}
+    if probed:
+        described += " (slowest buffer copied at %s GB/s)" % ", ".join(
+            "%s %s" % (k, v) for k, v in sorted(probed.items()))
     bufs.release()
     if pipelined:
         mode += ", copies pipelined per chunk"
@@ -641,7 +709,7 @@ def time_e2e(job, steps, world, host_alloc="thp", graph=True):
         mode += ", index call then attention in %d-query calls, copies pipelined" % E2E_SLICE
     else:
         mode += ", attention inputs up and sel down beside the calls"
-    return ms, h2d, d2h, mode
+    return ms, h2d, d2h, mode, described
 
 
 # ---------------------------------------------------------------- CPU arm --
@@ -851,10 +919,10 @@ def measure(name, args, world, rank):
     quality = selection_quality(job, args.quality_rows) \
         if args.quality_rows > 0 and job.mode == "sparse" else None
     if job.mode == "sparse":
-        e2e_ms, h2d, d2h, e2e_mode = time_e2e(job, max(1, min(args.steps, 3)), world,
-                                              args.host_alloc, graph=not args.no_graph)
+        e2e_ms, h2d, d2h, e2e_mode, host_desc = time_e2e(job, max(1, min(args.steps, 3)), world,
+                                                         args.host_alloc, graph=not args.no_graph)
     else:
-        e2e_ms, h2d, d2h, e2e_mode = None, 0, 0, None
+        e2e_ms, h2d, d2h, e2e_mode, host_desc = None, 0, 0, None, None
     cfg = {"workload": name, "batch": job.B, "ctx": job.L, "calls_per_step": len(job.calls),
            "queries_per_call": job.calls[0]["T"], "heads": H, "kv_heads": G, "head_dim": D,
            "index_dim": DI, "block": BLK, "topk": 16, "l2": "inputs larger than L2 (no flush)",
@@ -878,8 +946,7 @@ def measure(name, args, world, rank):
             "e2e": None if e2e_ms is None else {
                 "value": tokens / (e2e_ms / 1000.0), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "host_buffers": {"thp": "page-locked transparent huge pages",
-                                 "torch": "torch pinned allocator"}[args.host_alloc],
+                "host_buffers": host_desc,
                 "launch": e2e_mode},
             "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
             "selection_quality": quality}
@@ -926,9 +993,10 @@ def main():
                     help="comma-separated workloads reported in the same line (default: "
                          "prefill_128k,decode_256k when the workload is the default one; "
                          "'none' to skip)")
-    ap.add_argument("--host-alloc", choices=["thp", "torch"], default="thp",
-                    help="host buffers of the e2e leg: page-locked transparent huge pages "
-                         "(default) or torch's pinned allocator")
+    ap.add_argument("--host-alloc", choices=["auto", "thp", "torch"], default="auto",
+                    help="host buffers of the e2e leg: page-locked transparent huge pages, "
+                         "torch's pinned allocator, or (default) huge pages unless a probe "
+                         "copy shows the other kind faster")
     ap.add_argument("--quality-rows", type=int, default=64,
                     help="query positions sampled for the selection-quality figures (0: skip)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
