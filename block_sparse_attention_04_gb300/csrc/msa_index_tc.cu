@@ -21,11 +21,12 @@
 //               pairs; reducing tcgen05.ld of the row's 128 fp32 scores in
 //               16-column chunks (the load returns each chunk's maximum),
 //               block maximum, insertion into a
-//               register-resident top-15 (score desc, block id asc).
-// The [query x block] score matrix never leaves TMEM/registers.  At the end
-// of an item each warpgroup writes its rows' ranked top-15 of the blocks it
-// read (four lists per row and split); the k-way merge (topk_merge) combines
-// them, adds the local block and sorts.
+//               register-resident top-15 (score desc, block id asc); at
+//               the end of the item the four lists of a row merge in one
+//               parallel step (each candidate's rank among the 60).
+// The [query x block] score matrix never leaves TMEM/registers.  Each item
+// writes its rows' partial top-15 lists; the streaming path's k-way merge
+// (topk_merge) adds the local block and sorts.
 #include <climits>
 
 #include "msa_device.cuh"
@@ -42,7 +43,7 @@ constexpr int kPairKeys = 2 * kBlock;  // keys per MMA (N) and per accumulator s
 constexpr int kStages = 4;             // K_idx stages (two key blocks each) in flight
 constexpr int kAccStages = 2;          // TMEM accumulator stages of kPairKeys columns
 constexpr int kEpiWarps = 16;          // 4 warpgroups
-constexpr int kEpiLists = kEpiWarps / 4;  // ranked lists per (row, split): one per warpgroup
+constexpr int kEpiLists = kEpiWarps / 4;  // ranked lists per row at an item's end: one per warpgroup
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
 constexpr uint32_t kTmemCols = 512;
 constexpr int kItemRing = 4;           // item ids published by the copy thread, ahead of use
@@ -58,8 +59,9 @@ struct IdxCfg {
   static constexpr int kKSteps = DI / 16;
   static constexpr int kSmemA = 2 * kTileBytes;             // 2 buffers
   static constexpr int kSmemB = kStages * kStageBytes;
+  static constexpr int kSmemX = kEpiLists * kTileRows * kCand * 8;  // the lists at an item's end
   static constexpr int kSmemBar = 512;
-  static constexpr int kSmem = kSmemA + kSmemB + kSmemBar + 1024;  // + alignment
+  static constexpr int kSmem = kSmemA + kSmemB + kSmemX + kSmemBar + 1024;  // + alignment
 };
 
 struct IndexTcArgs {
@@ -151,20 +153,6 @@ __device__ __forceinline__ void list_insert_newest(float (&sc)[kCand], int (&id)
   }
 }
 
-// Insert (score, id) into a list sorted by (score desc, id asc).
-__device__ __forceinline__ void list_insert(float (&sc)[kCand], int (&id)[kCand], float cs, int ci) {
-#pragma unroll
-  for (int j = 0; j < kCand; ++j) {
-    const bool better = cs > sc[j] || (cs == sc[j] && ci < id[j]);
-    const float tsc = sc[j];
-    const int tid = id[j];
-    sc[j] = better ? cs : tsc;
-    id[j] = better ? ci : tid;
-    cs = better ? tsc : cs;
-    ci = better ? tid : ci;
-  }
-}
-
 template <int DI>
 __global__ void __launch_bounds__(kThreads, 1)
     index_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -174,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;                              // [abuf][128 rows][DI]
   uint8_t* sB = smem + C::kSmemA;                  // [stage][256 keys][DI]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + C::kSmemB);
+  Cand* sX = reinterpret_cast<Cand*>(sB + C::kSmemB);  // [kEpiLists][15][128 rows]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sX) + C::kSmemX);
   uint64_t* full = bars;                          // kStages
   uint64_t* empty = full + kStages;               // kStages
   uint64_t* a_full = empty + kStages;             // 2
@@ -441,18 +430,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (valid && blk < k1 && blk < lb && m > sc[kCand - 1]) list_insert_newest(sc, id, m, blk);
       }
       gstage += nst;
-      // each warpgroup writes its own ranked list (of the blocks it read):
-      // list sp * kEpiLists + wg of the row, merged with the others by
-      // topk_merge.  Merging the four lists here, through shared memory,
-      // kept the warpgroups from the next item's accumulator stages (the
-      // MMA warp's wait for tensor memory per stage was 220 instead of 158
-      // cycles at 128K, and 545 instead of 356 with the shorter items at 32K).
-      if (valid && ok) {
-        Cand* out = a.cand +
-                    ((((size_t)b * T + qi) * a.nsplit + sp) * kEpiLists + wg) * G * kCand +
-                    (size_t)g * kCand;
+      // Merge of the four warpgroups' lists of each row, in one parallel
+      // step: every list goes to shared memory, and each thread ranks its own
+      // 15 candidates among all 60 (its position in its list plus, for each
+      // other list, how many of its entries are better: a binary search, the
+      // lists being sorted).  Ranks of real candidates are distinct (block ids
+      // are), so the ranks below 15 fill the output once; empty entries rank
+      // after every real one and fill the remaining slots with equal values.
+      // Merging by serial insertion instead kept the epilogue from the next
+      // item's accumulator stages for most of 30,000 cycles per item.
 #pragma unroll
-        for (int j = 0; j < kCand; ++j) out[j] = Cand{sc[j], id[j]};
+      for (int j = 0; j < kCand; ++j) sX[(wg * kCand + j) * kTileRows + r] = Cand{sc[j], id[j]};
+      asm volatile("bar.sync 1, 512;" ::: "memory");
+      if (valid && ok) {
+        Cand* out = a.cand + ((((size_t)b * T + qi) * a.nsplit + sp) * G + g) * kCand;
+        // own candidates are read back from shared memory, so that the loop
+        // needs no run-time index into the register lists
+#pragma unroll 1
+        for (int j = 0; j < kCand; ++j) {
+          const Cand own = sX[(wg * kCand + j) * kTileRows + r];
+          const float cs = own.score;
+          const int ci = own.id;
+          int rank = j;
+#pragma unroll 1
+          for (int o = 1; o < kEpiLists; ++o) {
+            const Cand* x = sX + (((wg + o) % kEpiLists) * kCand) * kTileRows + r;
+            int lo = 0, hi = kCand;  // entries of list x better than (cs, ci): a prefix
+#pragma unroll
+            for (int step = 0; step < 4; ++step) {
+              const int mid = min((lo + hi) >> 1, kCand - 1);  // read stays in the list
+              const Cand c = x[mid * kTileRows];
+              const bool better = c.score > cs || (c.score == cs && c.id < ci);
+              if (lo < hi) {
+                lo = better ? mid + 1 : lo;
+                hi = better ? hi : mid;
+              }
+            }
+            rank += lo;
+          }
+          if (rank < kCand) out[rank] = Cand{cs, ci};
+        }
       }
       if (!ok || *abort_flag) *epi_stop = 1;
       asm volatile("bar.sync 1, 512;" ::: "memory");
@@ -480,8 +497,7 @@ int index_tc_npairs(const Shape& s) {
 
 // scratch layout: [candidate lists][item count (256 B)][items]
 size_t cand_bytes(const Shape& s) {
-  const size_t c = (size_t)s.B * s.T * index_tc_nsplit(s.max_blocks) * kEpiLists * s.G * kCand *
-                   sizeof(Cand);
+  const size_t c = (size_t)s.B * s.T * index_tc_nsplit(s.max_blocks) * s.G * kCand * sizeof(Cand);
   return (c + 255) / 256 * 256;
 }
 
@@ -538,7 +554,7 @@ cudaError_t launch_index_tc_impl(const Shape& s, const Positions& pos, const uin
   index_tc_kernel<DI><<<grid, kThreads, C::kSmem, st>>>(tm_q, tm_k, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_topk_merge(s, pos, 0, s.T, kSplitBlocks, a.nsplit, kEpiLists, ws.cand, sel, st);
+  return launch_topk_merge(s, pos, 0, s.T, kSplitBlocks, a.nsplit, ws.cand, sel, st);
 }
 
 }  // namespace

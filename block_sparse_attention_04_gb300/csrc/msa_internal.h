@@ -85,13 +85,10 @@ cudaError_t launch_index_stream(const Shape& s, const Positions& pos, int t0, in
                                 const Workspace& ws, cudaStream_t st);
 size_t index_stream_cand_entries(const Shape& s, int rows, int max_lb);
 
-// Merge of ranked candidate lists cand[(b,i)][nsplit][lps][G][15] into sel,
-// for queries [t0, t1): split j covers key blocks [j*bps, (j+1)*bps) and
-// holds lps lists (each of a disjoint subset of its blocks); a row reads the
-// lists of the splits below its local block.
+// Merge of per-split candidate lists cand[(b,i)][nsplit][G][15] (split j
+// covering key blocks [j*bps, (j+1)*bps)) into sel, for queries [t0, t1).
 cudaError_t launch_topk_merge(const Shape& s, const Positions& pos, int t0, int t1, int bps,
-                              int nsplit, int lps, const Cand* cand, int32_t* sel,
-                              cudaStream_t st);
+                              int nsplit, const Cand* cand, int32_t* sel, cudaStream_t st);
 
 cudaError_t launch_attn_stream(const Shape& s, const Positions& pos, int t0, int t1,
                                const uint16_t* q, const uint16_t* k, const uint16_t* v,

@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kIdxWarps * 32) index_stream_kernel(
 // ---------------------------------------------------------------------------
 // topk_merge: one warp per (pass row, group).
 __global__ void __launch_bounds__(256) topk_merge_kernel(
-    Shape s, Positions pos, int T, int t0, int Tp, int bps, int nsplit, int lps, int nrows,
+    Shape s, Positions pos, int T, int t0, int Tp, int bps, int nsplit, int nrows,
     const Cand* __restrict__ cand, int32_t* __restrict__ sel) {
   const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -197,10 +197,10 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(
   const int b = row / Tp, i = t0 + row % Tp;
   const int64_t t = (int64_t)pos.q_start[b] + i;
   const int lb = (int)(t / kBlock);
-  const int nvalid = lps * ((lb + bps - 1) / bps);  // lists of the splits that hold candidates
+  const int nvalid = (lb + bps - 1) / bps;
 
-  const Cand* base = cand + (size_t)row * nsplit * lps * s.G * kCand + (size_t)g * kCand;
-  const size_t lstride = (size_t)s.G * kCand;  // between consecutive lists of a row
+  const Cand* base = cand + (size_t)row * nsplit * s.G * kCand + (size_t)g * kCand;
+  const size_t lstride = (size_t)s.G * kCand;  // between the lists of consecutive splits
   int my_id = -1;
   if (nvalid == 1) {
     // one list: already the ranked top-15 of every candidate block
@@ -706,7 +706,7 @@ __global__ void dense_sel_kernel(Shape s, Positions pos, int chunk, int32_t* __r
 // times.  Same result as topk_merge_kernel; more rows in flight.
 constexpr int kSmallLists = 8;
 __global__ void __launch_bounds__(256) topk_merge_small_kernel(
-    Shape s, Positions pos, int T, int t0, int Tp, int bps, int nsplit, int lps, int nrows,
+    Shape s, Positions pos, int T, int t0, int Tp, int bps, int nsplit, int nrows,
     const Cand* __restrict__ cand, int32_t* __restrict__ sel) {
   const int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (gi >= (int64_t)nrows * s.G) return;
@@ -714,8 +714,8 @@ __global__ void __launch_bounds__(256) topk_merge_small_kernel(
   const int b = row / Tp, i = t0 + row % Tp;
   const int64_t t = (int64_t)pos.q_start[b] + i;
   const int lb = (int)(t / kBlock);
-  const int nvalid = lps * ((lb + bps - 1) / bps);
-  const Cand* base = cand + (size_t)row * nsplit * lps * s.G * kCand + (size_t)g * kCand;
+  const int nvalid = (lb + bps - 1) / bps;
+  const Cand* base = cand + (size_t)row * nsplit * s.G * kCand + (size_t)g * kCand;
   const size_t lstride = (size_t)s.G * kCand;
   float hs[kSmallLists];
   int hi[kSmallLists], cur[kSmallLists];
@@ -818,24 +818,23 @@ cudaError_t launch_index_stream(const Shape& s, const Positions& pos, int t0, in
       index_stream_kernel<32><<<grid, kIdxWarps * 32, 0, st>>>(s, pos, s.T, t0, Tp, bps, nsplit,
                                                                q_idx, k_idx, ws.cand, ws.status);
   }
-  return launch_topk_merge(s, pos, t0, t1, bps, nsplit > 0 ? nsplit : 1, 1, ws.cand, sel, st);
+  return launch_topk_merge(s, pos, t0, t1, bps, nsplit > 0 ? nsplit : 1, ws.cand, sel, st);
 }
 
 cudaError_t launch_topk_merge(const Shape& s, const Positions& pos, int t0, int t1, int bps,
-                              int nsplit, int lps, const Cand* cand, int32_t* sel,
-                              cudaStream_t st) {
+                              int nsplit, const Cand* cand, int32_t* sel, cudaStream_t st) {
   const int Tp = t1 - t0;
   const int rows = s.B * Tp;
   if (rows <= 0) return cudaSuccess;
   const int64_t warps = (int64_t)rows * s.G;
   const int max_lb = max_local_block(s, pos, t0, t1);
   note_launches(1);
-  if (lps * ((max_lb + bps - 1) / bps) <= kSmallLists)
+  if ((max_lb + bps - 1) / bps <= kSmallLists)
     topk_merge_small_kernel<<<(unsigned)((warps + 255) / 256), 256, 0, st>>>(
-        s, pos, s.T, t0, Tp, bps, nsplit, lps, rows, cand, sel);
+        s, pos, s.T, t0, Tp, bps, nsplit, rows, cand, sel);
   else
     topk_merge_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(s, pos, s.T, t0, Tp, bps,
-                                                                 nsplit, lps, rows, cand, sel);
+                                                                 nsplit, rows, cand, sel);
   return cudaGetLastError();
 }
 
